@@ -1,0 +1,408 @@
+"""Benchmark of the FP8 linear hot path on GB300.
+
+Workload (isolated FP8 linear, the reconstruction's timing table): N = 131072
+tokens through four linears I->O = 512->512, 512->2048, 2048->512, 512->8192,
+current tensorwise scaling, E4M3 X/W and E5M2 dY, fused dual-layout casts,
+weight quantization included (every step starts a new accumulation cycle),
+fprop + dgrad + wgrad with BF16 outputs.  One step = the four linears' forward
+and backward.  value = tokens processed by the linears per second
+(4 x 131072 per step), summed over ranks.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on the
+host cores on bounded token samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP8 linear fwd+bwd tokens/s; cast GB/s & GEMM TFLOP/s vs GB300 roofline"
+SHAPES = [(512, 512), (512, 2048), (2048, 512), (512, 8192)]   # (in K, out O)
+N_TOKENS = 131072
+RECIPE = "tensorwise"
+# RTX 4090 fused-layout FP8 medians of the four shapes (ms), the reconstruction's
+# isolated-linear table; another machine's numbers, reported as context only.
+PAGES_FUSED_MS = [2.0107, 5.4075, 5.4264, 22.7554]
+FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
+FP8_OVER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate ratio (4.5 / 2.25 PFLOP/s)
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.path is None or not os.path.exists(self.path):
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- dist
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    """Max over ranks (identity for one rank)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- oracle timing
+def oracle_tokens_per_s(n_sample: int, repeats: int = 1) -> tuple[float, float]:
+    """Time the CPU oracle's linear fwd+bwd over the four shapes on n_sample
+    tokens each; returns (tokens/s, seconds)."""
+    import oracle as o
+    from fp8_mixed_precision_gb300 import synthetic as syn
+    inputs = []
+    for i, (K, O) in enumerate(SHAPES):
+        x, w, dy = syn.linear_inputs(n_sample, K, O, layer=i)
+        inputs.append((syn.bits(x), syn.bits(w), syn.bits(dy)))
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        for x, w, dy in inputs:
+            o.linear_fwd_bwd(x, w, dy, RECIPE)
+    dt = time.perf_counter() - t0
+    return len(SHAPES) * n_sample * repeats / dt, dt
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle on bounded samples of the workload."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    # bounded sample per step, so that warmup + steps stay within minutes
+    n_sample = 256
+    for _ in range(args.warmup):
+        oracle_tokens_per_s(n_sample)
+    tps, dt = oracle_tokens_per_s(n_sample, repeats=args.steps)
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "isolated FP8 linear fwd+bwd, tensorwise, shapes "
+                   "512->512/512->2048/2048->512/512->8192",
+                   "tokens_per_step": len(SHAPES) * n_sample, "recipe": RECIPE},
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n_sample} tokens per linear per step (of {N_TOKENS})"},
+        "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import fp8_mixed_precision_gb300 as fp
+    from fp8_mixed_precision_gb300 import synthetic as syn
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fp.lib()
+
+    N = N_TOKENS
+    cache = fp.WeightCache()
+    layers = []
+    for i, (K, O) in enumerate(SHAPES):
+        x, w, dy = syn.linear_inputs(N, K, O, device=dev, layer=i)
+        h = cache.register(w, RECIPE)
+        layers.append(dict(K=K, O=O, x=x, w=w, dy=dy, h=h,
+                           y=torch.empty((N, O), dtype=torch.bfloat16, device=dev),
+                           dx=torch.empty((N, K), dtype=torch.bfloat16, device=dev),
+                           dw=torch.empty((O, K), dtype=torch.bfloat16, device=dev)))
+    ws = max((fp.linear_workspace(RECIPE, N, L["K"], L["O"], dev) for L in layers),
+             key=lambda t: t.numel())
+    ctx = max((fp.LinearContext(fp._empty_bytes(fp._ctx_bytes(RECIPE, N, L["K"]), dev), N, L["K"])
+               for L in layers), key=lambda c: c.ctx.numel())
+    version = [0]
+
+    def step():
+        cache.begin_cycle()
+        version[0] += 1
+        for L in layers:
+            cache.get(L["h"], version[0], True)
+            c = fp.LinearContext(ctx.ctx, N, L["K"])
+            fp.fp8_linear_fwd(L["x"], cache, L["h"], RECIPE, ws=ws, y=L["y"], ctx=c)
+            fp.fp8_linear_bwd(L["dy"], c, cache, L["h"], RECIPE, ws=ws, dx=L["dx"], dw=L["dw"])
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = fp.fp8_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    # ---- device-resident timing
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        n_launch0 = fp.fp8_launch_count()
+        fp.fp8_profile_begin()
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        kstats = fp.fp8_profile_end()
+        n_launch = fp.fp8_launch_count() - n_launch0
+    clocks = clk.summary()
+    ms_local = t0.elapsed_time(t1)
+    ms_total = reduce_max(ms_local, world, dev)
+    ms_step = ms_total / args.steps
+    tokens_per_step = len(SHAPES) * N
+    value = world * tokens_per_step / (ms_step / 1e3)
+
+    # ---- roofline of the dominant kernel
+    peaks = _peaks()
+    fp8_peak = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
+    kstats.sort(key=lambda k: -k["total_ms"])
+    tot_ms = sum(k["total_ms"] for k in kstats) or 1.0
+    kernels = []
+    for k in kstats:
+        gbs = k["bytes"] / (k["total_ms"] / 1e3) / 1e9
+        tfs = k["flops"] / (k["total_ms"] / 1e3) / 1e12
+        kernels.append({"name": k["name"], "launches": k["launches"] // args.steps,
+                        "ms_per_step": k["total_ms"] / args.steps,
+                        "share": k["total_ms"] / tot_ms, "GB/s": gbs, "TFLOP/s": tfs,
+                        "hbm_frac": gbs / peaks["hbm_gbs"]})
+    dom = kstats[0]
+    dom_t = dom["total_ms"] / dom["launches"] / 1e3
+    intensity = dom["flops"] / max(dom["bytes"], 1.0)
+    ridge = fp8_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if intensity > ridge:
+        achieved = dom["flops"] / dom["launches"] / dom_t / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s"}
+    else:
+        achieved = dom["bytes"] / dom["launches"] / dom_t / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = dom["name"]
+    roof["peak_source"] = peaks["source"] + (" sustained bf16 x 2" if roof["bound"] == "tensor"
+                                             else " copy bandwidth")
+    roof["traffic"] = _traffic_for(dom["name"])
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = run_e2e(fp, layers, cache, ws, ctx, N, dev, world, args, stream)
+
+    # ---- CPU baseline (rank 0, one GPU only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_s = 2048
+        tps, dt = oracle_tokens_per_s(n_s)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{n_s} tokens per linear (of {N_TOKENS}), all four shapes, once; "
+                         f"{dt:.1f} s"}
+
+    pages_tps = tokens_per_step / (sum(PAGES_FUSED_MS) / 1e3)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": value / pages_tps,
+            "dtype": "fp8 (e4m3/e5m2) x fp8 -> f32 accumulate -> bf16",
+            "data": "synthetic (seeded normal bf16: X~N(0,1), W~N(0,0.02), dY~N(0,1e-3))",
+            "config": {"workload": "isolated FP8 linear fwd+bwd, N=131072 tokens, shapes "
+                                   "512->512/512->2048/2048->512/512->8192, tensorwise current "
+                                   "scaling, fused dual-layout casts, weight quantized every step",
+                       "tokens_per_step": tokens_per_step, "recipe": RECIPE,
+                       "l2": "inputs larger than L2 (about 9 GB touched per step)",
+                       "parallelism": f"dp{world} (replicas, no collective)"},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": n_launch,
+            "clocks": clocks,
+            "kernels": kernels,
+            "baseline_note": "vs_baseline divides by the RTX 4090 fused-layout FP8 figures of "
+                             "the reconstruction's table (context only)",
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def _traffic_for(name):
+    """DRAM bytes per launch from a committed ncu summary, when it still
+    matches the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        import hashlib
+        h = hashlib.sha256()
+        for fn in sorted(os.listdir(os.path.join(ROOT, "fp8_mixed_precision_gb300", "csrc"))):
+            with open(os.path.join(ROOT, "fp8_mixed_precision_gb300", "csrc", fn), "rb") as f:
+                h.update(f.read())
+        if d.get("csrc_sha256") != h.hexdigest():
+            return None
+        return d.get("kernels", {}).get(name, {}).get("dram_bytes_per_launch")
+    except (OSError, ValueError, KeyError):
+        return None
+
+
+def run_e2e(fp, layers, cache, ws, ctx, N, dev, world, args, stream):
+    """Same step through the C ABI with inputs copied from pinned host memory
+    and outputs copied back inside the timed region."""
+    import torch
+    host = []
+    h2d = d2h = 0
+    for L in layers:
+        hx = torch.empty(L["x"].shape, dtype=torch.bfloat16, pin_memory=True)
+        hw = torch.empty(L["w"].shape, dtype=torch.bfloat16, pin_memory=True)
+        hdy = torch.empty(L["dy"].shape, dtype=torch.bfloat16, pin_memory=True)
+        hx.copy_(L["x"]); hw.copy_(L["w"]); hdy.copy_(L["dy"])
+        hy = torch.empty(L["y"].shape, dtype=torch.bfloat16, pin_memory=True)
+        hdx = torch.empty(L["dx"].shape, dtype=torch.bfloat16, pin_memory=True)
+        hdw = torch.empty(L["dw"].shape, dtype=torch.bfloat16, pin_memory=True)
+        host.append((hx, hw, hdy, hy, hdx, hdw))
+        h2d += 2 * (hx.numel() + hw.numel() + hdy.numel())
+        d2h += 2 * (hy.numel() + hdx.numel() + hdw.numel())
+    version = [10 ** 6]
+
+    def step():
+        cache.begin_cycle()
+        version[0] += 1
+        for L, (hx, hw, hdy, hy, hdx, hdw) in zip(layers, host):
+            L["x"].copy_(hx, non_blocking=True)
+            L["w"].copy_(hw, non_blocking=True)
+            L["dy"].copy_(hdy, non_blocking=True)
+            cache.get(L["h"], version[0], True)
+            c = fp.LinearContext(ctx.ctx, N, L["K"])
+            fp.fp8_linear_fwd(L["x"], cache, L["h"], RECIPE, ws=ws, y=L["y"], ctx=c)
+            fp.fp8_linear_bwd(L["dy"], c, cache, L["h"], RECIPE, ws=ws, dx=L["dx"], dw=L["dw"])
+            hy.copy_(L["y"], non_blocking=True)
+            hdx.copy_(L["dx"], non_blocking=True)
+            hdw.copy_(L["dw"], non_blocking=True)
+
+    k = max(3, min(args.steps, 20))
+    step()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(k):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = reduce_max(t0.elapsed_time(t1), world, dev) / k
+    value = world * len(SHAPES) * N / (ms / 1e3)
+    return {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": k, "ms_per_step": ms}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,503 @@
+// C-ABI layer of the FP8 linear library: argument validation, workspace
+// carving, the weight cache (is_first_microbatch semantics) and the
+// orchestration of quantize + GEMM calls for the linear layer's forward and
+// backward.  Host code only; every arithmetic step runs in the kernels.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/fp8lin.h"
+#include "internal.h"
+
+namespace fp8lin {
+static std::atomic<uint64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+// ---- per-kernel event timing (fp8_profile_begin / fp8_profile_end)
+namespace {
+struct ProfRec {
+  const char *name;
+  cudaEvent_t start, stop;
+  double bytes, flops;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+}  // namespace
+
+LaunchScope::LaunchScope(const char *name, cudaStream_t st, double bytes, double flops)
+    : st_(st) {
+  count_launch();
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof_on) return;
+  ProfRec r{name, take_event(), take_event(), bytes, flops};
+  if (!r.start || !r.stop) return;
+  cudaEventRecord(r.start, st);
+  g_prof.push_back(r);
+  rec_ = (int)g_prof.size() - 1;
+}
+
+LaunchScope::~LaunchScope() {
+  if (rec_ < 0) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (rec_ < (int)g_prof.size()) cudaEventRecord(g_prof[rec_].stop, st_);
+}
+}  // namespace fp8lin
+
+using namespace fp8lin;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+inline cudaStream_t cs(fp8_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+fp8_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA; }
+
+int format_of(fp8_role role) { return role == FP8_ROLE_GRAD ? FP8_FORMAT_E5M2 : FP8_FORMAT_E4M3; }
+
+// 0 tensorwise, 1 1x128, 2 128x128
+int qmode_of(fp8_recipe recipe, fp8_role role) {
+  if (recipe == FP8_RECIPE_TENSORWISE) return 0;
+  return role == FP8_ROLE_WEIGHT ? 2 : 1;
+}
+
+bool valid_recipe(int r) { return r == FP8_RECIPE_TENSORWISE || r == FP8_RECIPE_BLOCK; }
+bool valid_role(int r) { return r >= FP8_ROLE_ACT && r <= FP8_ROLE_GRAD; }
+
+fp8_status check_dims(int64_t a, int64_t b) {
+  if (a < 0 || b < 0) return FP8_ERR_INVALID_ARG;
+  if (a % 16 || b % 16) return FP8_ERR_SHAPE;
+  if (a > (int64_t(1) << 31) || b > (int64_t(1) << 31)) return FP8_ERR_SHAPE;
+  return FP8_OK;
+}
+
+// number of floats in one scale array of a layout
+int64_t scale_elems(fp8_recipe recipe, fp8_role role, int64_t rows, int64_t cols, int colwise) {
+  int64_t sr = 0, sc = 0;
+  fp8_scale_shape(recipe, role, rows, cols, colwise, &sr, &sc);
+  return sr * sc;
+}
+
+// Carves consecutive 256-byte-aligned regions out of a base pointer.
+struct Carver {
+  uint8_t *base;
+  size_t off = 0;
+  explicit Carver(void *b) : base(static_cast<uint8_t *>(b)) {}
+  template <class T>
+  T *take(size_t bytes) {
+    T *p = base ? reinterpret_cast<T *>(base + off) : nullptr;
+    off += align_up(bytes);
+    return p;
+  }
+};
+
+}  // namespace
+
+extern "C" {
+
+const char *fp8_status_string(fp8_status s) {
+  switch (s) {
+    case FP8_OK: return "ok";
+    case FP8_ERR_INVALID_ARG: return "invalid argument";
+    case FP8_ERR_SHAPE: return "unsupported shape (dimensions must be multiples of 16)";
+    case FP8_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case FP8_ERR_STALE: return "weight-cache entry stale or version changed mid-cycle";
+    case FP8_ERR_TIMEOUT: return "device-side wait timed out";
+    case FP8_ERR_CUDA: return "CUDA error";
+    case FP8_ERR_UNSUPPORTED: return "unsupported";
+    case FP8_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+uint64_t fp8_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+fp8_status fp8_scale_shape(fp8_recipe recipe, fp8_role role, int64_t rows, int64_t cols,
+                           int colwise, int64_t *srows, int64_t *scols) {
+  if (!srows || !scols || !valid_recipe(recipe) || !valid_role(role)) return FP8_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0) return FP8_ERR_INVALID_ARG;
+  const int mode = qmode_of(recipe, role);
+  if (mode == 0) {
+    *srows = 1;
+    *scols = 1;
+  } else if (mode == 1) {
+    *srows = colwise ? cols : rows;
+    *scols = colwise ? cdiv(rows, 128) : cdiv(cols, 128);
+  } else {
+    *srows = colwise ? cdiv(cols, 128) : cdiv(rows, 128);
+    *scols = colwise ? cdiv(rows, 128) : cdiv(cols, 128);
+  }
+  return FP8_OK;
+}
+
+fp8_status fp8_quantize_workspace_size(fp8_recipe recipe, int64_t rows, int64_t cols,
+                                       size_t *bytes) {
+  if (!bytes || !valid_recipe(recipe) || rows < 0 || cols < 0) return FP8_ERR_INVALID_ARG;
+  *bytes = recipe == FP8_RECIPE_TENSORWISE ? (size_t)kMaxPartials * sizeof(float) : 0;
+  return FP8_OK;
+}
+
+fp8_status fp8_quantize(const void *x, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_role role,
+                        uint8_t *rowwise_out, uint8_t *colwise_out, float *row_scale,
+                        float *row_scale_inv, float *col_scale, float *col_scale_inv,
+                        void *workspace, size_t workspace_bytes, fp8_stream_t stream) {
+  if (!valid_recipe(recipe) || !valid_role(role)) return FP8_ERR_INVALID_ARG;
+  fp8_status st = check_dims(rows, cols);
+  if (st != FP8_OK) return st;
+  if (!rowwise_out && !colwise_out) return FP8_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return FP8_OK;
+  if (!x) return FP8_ERR_INVALID_ARG;
+  const int mode = qmode_of(recipe, role);
+  if ((rowwise_out || mode == 0) && (!row_scale || !row_scale_inv)) return FP8_ERR_INVALID_ARG;
+  if (colwise_out && mode != 0 && (!col_scale || !col_scale_inv)) return FP8_ERR_INVALID_ARG;
+  if (mode != 0 && !rowwise_out) row_scale = row_scale_inv = nullptr;
+  if (mode == 0 && (!col_scale || !col_scale_inv)) col_scale = col_scale_inv = nullptr;
+  if (!aligned16(x) || (rowwise_out && !aligned16(rowwise_out)) ||
+      (colwise_out && !aligned16(colwise_out)))
+    return FP8_ERR_ALIGN;
+  size_t need = 0;
+  fp8_quantize_workspace_size(recipe, rows, cols, &need);
+  if (workspace_bytes < need || (need && !workspace)) return FP8_ERR_WORKSPACE;
+  return from_cuda(launch_quantize(x, rows, cols, mode, format_of(role), rowwise_out, colwise_out,
+                                   row_scale, row_scale_inv, col_scale, col_scale_inv,
+                                   static_cast<float *>(workspace), cs(stream)));
+}
+
+fp8_status fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, fp8_scaling scaling,
+                                   size_t *bytes) {
+  if (!bytes || M < 0 || N < 0 || K < 0 || scaling < 0 || scaling > 2) return FP8_ERR_INVALID_ARG;
+  *bytes = gemm_workspace_bytes(M, N, K, scaling);
+  return FP8_OK;
+}
+
+fp8_status fp8_gemm(const uint8_t *A, fp8_format a_fmt, const float *a_scale_inv, const uint8_t *B,
+                    fp8_format b_fmt, const float *b_scale_inv, int64_t M, int64_t N, int64_t K,
+                    fp8_scaling scaling, void *C, void *workspace, size_t workspace_bytes,
+                    fp8_stream_t stream) {
+  if (scaling < 0 || scaling > 2 || (a_fmt != 0 && a_fmt != 1) || (b_fmt != 0 && b_fmt != 1))
+    return FP8_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0) return FP8_ERR_INVALID_ARG;
+  if (M % 16 || N % 16 || K % 16) return FP8_ERR_SHAPE;
+  if (M == 0 || N == 0) return FP8_OK;
+  if (!C || (K > 0 && (!A || !B || !a_scale_inv || !b_scale_inv))) return FP8_ERR_INVALID_ARG;
+  if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B)))) return FP8_ERR_ALIGN;
+  const size_t need = gemm_workspace_bytes(M, N, K, scaling);
+  if (workspace_bytes < need || (need && !workspace)) return FP8_ERR_WORKSPACE;
+  if (need && !aligned16(workspace)) return FP8_ERR_ALIGN;
+  return from_cuda(launch_gemm(A, a_fmt, a_scale_inv, B, b_fmt, b_scale_inv, M, N, K, scaling, C,
+                               workspace, cs(stream)));
+}
+
+// ---------------------------------------------------------------- weight cache
+struct fp8_weight_cache {
+  struct Entry {
+    const void *w;
+    int64_t O, K;
+    fp8_recipe recipe;
+    uint8_t *w_row, *w_col;
+    float *row_scale, *row_scale_inv, *col_scale, *col_scale_inv;
+    void *ws;
+    size_t ws_bytes;
+    uint64_t cycle;    // cycle in which the FP8 copy was last made (0 = never)
+    uint64_t version;  // caller's weight version at that time
+  };
+  std::vector<Entry> entries;
+  uint64_t cycle = 1;
+};
+
+fp8_status fp8_weight_cache_create(fp8_weight_cache **out) {
+  if (!out) return FP8_ERR_INVALID_ARG;
+  *out = new (std::nothrow) fp8_weight_cache();
+  return *out ? FP8_OK : FP8_ERR_INVALID_ARG;
+}
+
+void fp8_weight_cache_destroy(fp8_weight_cache *cache) { delete cache; }
+
+fp8_status fp8_weight_cache_register(fp8_weight_cache *cache, const void *w, int64_t O, int64_t K,
+                                     fp8_recipe recipe, uint8_t *w_row, uint8_t *w_col,
+                                     float *row_scale, float *row_scale_inv, float *col_scale,
+                                     float *col_scale_inv, void *workspace, size_t workspace_bytes,
+                                     fp8_weight_handle *out) {
+  if (!cache || !out || !valid_recipe(recipe)) return FP8_ERR_INVALID_ARG;
+  fp8_status st = check_dims(O, K);
+  if (st != FP8_OK) return st;
+  if (O == 0 || K == 0) return FP8_ERR_SHAPE;
+  if (!w || !w_row || !w_col || !row_scale || !row_scale_inv || !col_scale || !col_scale_inv)
+    return FP8_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(w_row) || !aligned16(w_col)) return FP8_ERR_ALIGN;
+  size_t need = 0;
+  fp8_quantize_workspace_size(recipe, O, K, &need);
+  if (workspace_bytes < need || (need && !workspace)) return FP8_ERR_WORKSPACE;
+  fp8_weight_cache::Entry e{w, O, K, recipe, w_row, w_col, row_scale, row_scale_inv,
+                            col_scale, col_scale_inv, workspace, workspace_bytes, 0, 0};
+  cache->entries.push_back(e);
+  *out = (fp8_weight_handle)(cache->entries.size() - 1);
+  return FP8_OK;
+}
+
+fp8_status fp8_weight_cache_begin_cycle(fp8_weight_cache *cache) {
+  if (!cache) return FP8_ERR_INVALID_ARG;
+  ++cache->cycle;
+  return FP8_OK;
+}
+
+fp8_status fp8_weight_cache_get(fp8_weight_cache *cache, fp8_weight_handle h, uint64_t w_version,
+                                int use_cache, fp8_stream_t stream, int *requantized) {
+  if (requantized) *requantized = 0;
+  if (!cache || h < 0 || (size_t)h >= cache->entries.size()) return FP8_ERR_INVALID_ARG;
+  auto &e = cache->entries[h];
+  if (use_cache && e.cycle == cache->cycle) {
+    if (e.version != w_version) return FP8_ERR_STALE;
+    return FP8_OK;  // is_first_microbatch=False: reuse the FP8 copy
+  }
+  fp8_status st = fp8_quantize(e.w, e.O, e.K, e.recipe, FP8_ROLE_WEIGHT, e.w_row, e.w_col,
+                               e.row_scale, e.row_scale_inv, e.col_scale, e.col_scale_inv, e.ws,
+                               e.ws_bytes, stream);
+  if (st != FP8_OK) return st;
+  e.cycle = cache->cycle;
+  e.version = w_version;
+  if (requantized) *requantized = 1;
+  return FP8_OK;
+}
+
+// ---------------------------------------------------------------- linear layer
+namespace {
+
+struct CtxLayout {
+  size_t xq_col, scale, scale_inv, total;
+};
+CtxLayout ctx_layout(fp8_recipe recipe, int64_t N, int64_t K) {
+  CtxLayout L;
+  const int64_t ns = scale_elems(recipe, FP8_ROLE_ACT, N, K, 1);
+  L.xq_col = 0;
+  L.scale = align_up((size_t)N * K);
+  L.scale_inv = L.scale + align_up((size_t)ns * 4);
+  L.total = L.scale_inv + align_up((size_t)ns * 4);
+  return L;
+}
+
+fp8_scaling fwd_scaling(fp8_recipe r) {
+  return r == FP8_RECIPE_TENSORWISE ? FP8_SCALING_TENSOR : FP8_SCALING_1x128_128x128;
+}
+fp8_scaling wgrad_scaling(fp8_recipe r) {
+  return r == FP8_RECIPE_TENSORWISE ? FP8_SCALING_TENSOR : FP8_SCALING_1x128_1x128;
+}
+
+size_t fwd_ws(fp8_recipe r, int64_t N, int64_t K, int64_t O) {
+  const int64_t ns = scale_elems(r, FP8_ROLE_ACT, N, K, 0);
+  size_t qws = 0;
+  fp8_quantize_workspace_size(r, N, K, &qws);
+  return align_up((size_t)N * K) + 2 * align_up((size_t)ns * 4) + align_up(qws) +
+         align_up(gemm_workspace_bytes(N, O, K, fwd_scaling(r)));
+}
+size_t bwd_ws(fp8_recipe r, int64_t N, int64_t K, int64_t O) {
+  const int64_t nr = scale_elems(r, FP8_ROLE_GRAD, N, O, 0);
+  const int64_t nc = scale_elems(r, FP8_ROLE_GRAD, N, O, 1);
+  size_t qws = 0;
+  fp8_quantize_workspace_size(r, N, O, &qws);
+  const size_t g = std::max(gemm_workspace_bytes(N, K, O, fwd_scaling(r)),
+                            gemm_workspace_bytes(O, K, N, wgrad_scaling(r)));
+  return 2 * align_up((size_t)N * O) + 2 * align_up((size_t)nr * 4) + 2 * align_up((size_t)nc * 4) +
+         align_up(qws) + align_up(g);
+}
+
+}  // namespace
+
+fp8_status fp8_linear_ctx_size(fp8_recipe recipe, int64_t N, int64_t K, size_t *bytes) {
+  if (!bytes || !valid_recipe(recipe) || N < 0 || K < 0) return FP8_ERR_INVALID_ARG;
+  *bytes = ctx_layout(recipe, N, K).total;
+  return FP8_OK;
+}
+
+fp8_status fp8_linear_workspace_size(fp8_recipe recipe, int64_t N, int64_t K, int64_t O,
+                                     size_t *bytes) {
+  if (!bytes || !valid_recipe(recipe) || N < 0 || K < 0 || O < 0) return FP8_ERR_INVALID_ARG;
+  *bytes = std::max(fwd_ws(recipe, N, K, O), bwd_ws(recipe, N, K, O));
+  return FP8_OK;
+}
+
+fp8_status fp8_linear_fwd(const void *X, int64_t N, int64_t K, fp8_weight_cache *cache,
+                          fp8_weight_handle h, fp8_recipe recipe, void *Y, void *ctx, void *ws,
+                          size_t ws_bytes, fp8_stream_t stream) {
+  if (!cache || h < 0 || (size_t)h >= cache->entries.size() || !valid_recipe(recipe))
+    return FP8_ERR_INVALID_ARG;
+  const auto &e = cache->entries[h];
+  if (e.recipe != recipe || e.K != K) return FP8_ERR_INVALID_ARG;
+  fp8_status st = check_dims(N, K);
+  if (st != FP8_OK) return st;
+  if (e.cycle != cache->cycle) return FP8_ERR_STALE;
+  if (N == 0) return FP8_OK;
+  if (!X || !Y || !ctx || !ws) return FP8_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(Y) || !aligned16(ctx) || !aligned16(ws)) return FP8_ERR_ALIGN;
+  const int64_t O = e.O;
+  if (ws_bytes < fwd_ws(recipe, N, K, O)) return FP8_ERR_WORKSPACE;
+  const CtxLayout L = ctx_layout(recipe, N, K);
+  uint8_t *c = static_cast<uint8_t *>(ctx);
+  const int64_t ns = scale_elems(recipe, FP8_ROLE_ACT, N, K, 0);
+  size_t qws = 0;
+  fp8_quantize_workspace_size(recipe, N, K, &qws);
+  Carver w(ws);
+  uint8_t *xq_row = w.take<uint8_t>((size_t)N * K);
+  float *rs = w.take<float>((size_t)ns * 4);
+  float *rsi = w.take<float>((size_t)ns * 4);
+  float *part = w.take<float>(qws);
+  void *gws = w.take<void>(gemm_workspace_bytes(N, O, K, fwd_scaling(recipe)));
+  st = fp8_quantize(X, N, K, recipe, FP8_ROLE_ACT, xq_row, c + L.xq_col, rs, rsi,
+                    reinterpret_cast<float *>(c + L.scale), reinterpret_cast<float *>(c + L.scale_inv),
+                    part, qws, stream);
+  if (st != FP8_OK) return st;
+  return fp8_gemm(xq_row, FP8_FORMAT_E4M3, rsi, e.w_row, FP8_FORMAT_E4M3, e.row_scale_inv, N, O, K,
+                  fwd_scaling(recipe), Y, gws, gemm_workspace_bytes(N, O, K, fwd_scaling(recipe)),
+                  stream);
+}
+
+fp8_status fp8_linear_bwd(const void *dY, int64_t N, int64_t O, const void *ctx,
+                          fp8_weight_cache *cache, fp8_weight_handle h, fp8_recipe recipe, void *dX,
+                          void *dW, void *ws, size_t ws_bytes, fp8_stream_t stream) {
+  if (!cache || h < 0 || (size_t)h >= cache->entries.size() || !valid_recipe(recipe))
+    return FP8_ERR_INVALID_ARG;
+  const auto &e = cache->entries[h];
+  if (e.recipe != recipe || e.O != O) return FP8_ERR_INVALID_ARG;
+  fp8_status st = check_dims(N, O);
+  if (st != FP8_OK) return st;
+  if (e.cycle != cache->cycle) return FP8_ERR_STALE;
+  const int64_t K = e.K;
+  if (N == 0) return FP8_OK;  // dW of an empty batch is not written
+  if (!dY || !ctx || !dW || !ws) return FP8_ERR_INVALID_ARG;
+  if (!aligned16(dY) || !aligned16(ctx) || !aligned16(dW) || !aligned16(ws) ||
+      (dX && !aligned16(dX)))
+    return FP8_ERR_ALIGN;
+  if (ws_bytes < bwd_ws(recipe, N, K, O)) return FP8_ERR_WORKSPACE;
+  const CtxLayout L = ctx_layout(recipe, N, K);
+  const uint8_t *c = static_cast<const uint8_t *>(ctx);
+  const int64_t nr = scale_elems(recipe, FP8_ROLE_GRAD, N, O, 0);
+  const int64_t nc = scale_elems(recipe, FP8_ROLE_GRAD, N, O, 1);
+  size_t qws = 0;
+  fp8_quantize_workspace_size(recipe, N, O, &qws);
+  const size_t gbytes = std::max(gemm_workspace_bytes(N, K, O, fwd_scaling(recipe)),
+                                 gemm_workspace_bytes(O, K, N, wgrad_scaling(recipe)));
+  Carver w(ws);
+  uint8_t *g_row = w.take<uint8_t>((size_t)N * O);
+  uint8_t *g_col = w.take<uint8_t>((size_t)N * O);
+  float *grs = w.take<float>((size_t)nr * 4);
+  float *grsi = w.take<float>((size_t)nr * 4);
+  float *gcs = w.take<float>((size_t)nc * 4);
+  float *gcsi = w.take<float>((size_t)nc * 4);
+  float *part = w.take<float>(qws);
+  void *gws = w.take<void>(gbytes);
+  st = fp8_quantize(dY, N, O, recipe, FP8_ROLE_GRAD, g_row, g_col, grs, grsi, gcs, gcsi, part, qws,
+                    stream);
+  if (st != FP8_OK) return st;
+  if (dX) {
+    st = fp8_gemm(g_row, FP8_FORMAT_E5M2, grsi, e.w_col, FP8_FORMAT_E4M3, e.col_scale_inv, N, K, O,
+                  fwd_scaling(recipe), dX, gws, gbytes, stream);
+    if (st != FP8_OK) return st;
+  }
+  return fp8_gemm(g_col, FP8_FORMAT_E5M2, gcsi, c + L.xq_col, FP8_FORMAT_E4M3,
+                  reinterpret_cast<const float *>(c + L.scale_inv), O, K, N, wgrad_scaling(recipe),
+                  dW, gws, gbytes, stream);
+}
+
+// ---------------------------------------------------------------- glue + status
+fp8_status fp8_gelu_fwd(const void *H, void *A, int64_t n, fp8_stream_t stream) {
+  if (n < 0) return FP8_ERR_INVALID_ARG;
+  if (n % 8) return FP8_ERR_SHAPE;
+  if (n == 0) return FP8_OK;
+  if (!H || !A) return FP8_ERR_INVALID_ARG;
+  if (!aligned16(H) || !aligned16(A)) return FP8_ERR_ALIGN;
+  return from_cuda(launch_gelu_fwd(H, A, n, cs(stream)));
+}
+
+fp8_status fp8_gelu_bwd(const void *dA, const void *H, void *dH, int64_t n, fp8_stream_t stream) {
+  if (n < 0) return FP8_ERR_INVALID_ARG;
+  if (n % 8) return FP8_ERR_SHAPE;
+  if (n == 0) return FP8_OK;
+  if (!dA || !H || !dH) return FP8_ERR_INVALID_ARG;
+  if (!aligned16(dA) || !aligned16(H) || !aligned16(dH)) return FP8_ERR_ALIGN;
+  return from_cuda(launch_gelu_bwd(dA, H, dH, n, cs(stream)));
+}
+
+fp8_status fp8_grad_accumulate(float *acc, const void *dW, int64_t n, fp8_stream_t stream) {
+  if (n < 0) return FP8_ERR_INVALID_ARG;
+  if (n % 8) return FP8_ERR_SHAPE;
+  if (n == 0) return FP8_OK;
+  if (!acc || !dW) return FP8_ERR_INVALID_ARG;
+  if (!aligned16(acc) || !aligned16(dW)) return FP8_ERR_ALIGN;
+  return from_cuda(launch_grad_accumulate(acc, dW, n, cs(stream)));
+}
+
+fp8_status fp8_profile_begin(void) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (auto &r : g_prof) {
+    g_event_pool.push_back(r.start);
+    g_event_pool.push_back(r.stop);
+  }
+  g_prof.clear();
+  g_prof_on = true;
+  return FP8_OK;
+}
+
+fp8_status fp8_profile_end(fp8_kernel_stat *out, int cap, int *n) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = false;
+  std::map<std::string, fp8_kernel_stat> agg;
+  fp8_status st = FP8_OK;
+  for (auto &r : g_prof) {
+    float ms = 0.0f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess) {
+      st = FP8_ERR_CUDA;
+      continue;
+    }
+    fp8_kernel_stat &k = agg[r.name];
+    if (k.launches == 0) {
+      std::memset(&k, 0, sizeof(k));
+      std::strncpy(k.name, r.name, sizeof(k.name) - 1);
+    }
+    k.launches += 1;
+    k.total_ms += ms;
+    k.bytes += r.bytes;
+    k.flops += r.flops;
+  }
+  for (auto &r : g_prof) {
+    g_event_pool.push_back(r.start);
+    g_event_pool.push_back(r.stop);
+  }
+  g_prof.clear();
+  if (n) *n = (int)agg.size();
+  int i = 0;
+  for (auto &kv : agg) {
+    if (out && i < cap) out[i] = kv.second;
+    ++i;
+  }
+  return st;
+}
+
+fp8_status fp8_get_device_status(fp8_stream_t stream) {
+  unsigned s = 0;
+  if (gemm_read_status(&s, cs(stream)) != cudaSuccess) return FP8_ERR_CUDA;
+  return (fp8_status)s;
+}
+
+}  // extern "C"

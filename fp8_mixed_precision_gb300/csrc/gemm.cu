@@ -1,0 +1,519 @@
+// FP8 GEMM on the sm_103a 5th-generation tensor cores.
+//
+//   C[M, N] = sum_k (A[m, k] * sa) * (B[n, k] * sb),   A, B K-major FP8, C bf16
+//
+// Used for the fprop, dgrad and wgrad GEMMs of the FP8 linear layer
+// ("Native FP8 MLP reconstruction", implementation paragraph: FP8 operands,
+// BF16 GEMM outputs, use_fast_accum=False).  fp32 accumulation throughout:
+//   FP8_SCALING_TENSOR        one accumulator over the whole K range in TMEM,
+//                             scaled by sa*sb in the epilogue;
+//   FP8_SCALING_1x128_*       every 128-deep K block is accumulated into a
+//                             fresh TMEM partial; the epilogue warps multiply
+//                             it by that block's scales and add it to an fp32
+//                             register accumulator (software promotion).
+//
+// Structure: persistent CTAs (one per SM), warp-specialised.
+//   warp 0      TMA producer: 128x128-byte A and B tiles (128B swizzle) into a
+//               kStages-deep shared-memory ring guarded by full/empty mbarriers
+//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
+//               (kind::f8f6f4, M=128, N=128, K=32 per instruction)
+//   warps 2-9   epilogue: tcgen05.ld from TMEM, scale, round to bf16, store.
+//               Warp w reads TMEM lanes 32*(w%4)..+31 and column half (w-2)/4.
+// The MMA writes two TMEM buffers alternately so the epilogue of one tile
+// (tensor scaling) or of one K block (block scaling) overlaps the next MMAs.
+// Split-K (small M*N, deep K): each split writes an fp32 partial to the
+// workspace; a second kernel sums the splits in a fixed order.  Every wait is
+// bounded: on expiry the kernel records FP8_ERR_TIMEOUT, drains what it has in
+// flight, frees its TMEM and returns.
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8lin {
+
+namespace {
+
+constexpr int BM = 128, BN = 128, BK = 128;
+constexpr int kStages = 6;
+constexpr int kStageA = BM * BK;  // bytes
+constexpr int kStageB = BN * BK;
+constexpr int kStageBytes = kStageA + kStageB;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr uint32_t kTmemCols = 2 * BN;  // two fp32 accumulator buffers
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+constexpr uint64_t kDrainLimitNs = 100000000ull;   // 0.1 s
+constexpr int kSplitTargetCtas = 152;              // split-K fills about this many CTAs
+
+__device__ unsigned g_gemm_status;
+
+struct GemmArgs {
+  int64_t M, N, K;
+  int tiles_m, tiles_n, kbs, splits, kb_per_split;
+  int64_t units;
+  const float *a_sinv;
+  const float *b_sinv;
+  int64_t lds_a, lds_b;  // row strides (floats) of the block scale arrays
+  void *out;             // bf16 C [M, N], or fp32 partials [splits, M, N]
+  uint32_t idesc;
+};
+
+struct SmemCtl {
+  uint64_t full[kStages], empty[kStages];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+  float bscale[kEpiWarps][64];
+};
+
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + sizeof(SmemCtl);
+
+// Bounded wait on phase `parity` of `bar`; false on abort or timeout.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 63) == 0) {
+      if (*abort) return false;
+      if (ptx::globaltimer() - t0 > kWaitLimitNs) {
+        atomicCAS(&g_gemm_status, 0u, (unsigned)FP8_ERR_TIMEOUT);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag (used only to drain in-flight work).
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+  const uint64_t t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait(bar, parity))
+    if (ptx::globaltimer() - t0 > kDrainLimitNs) {
+      atomicCAS(&g_gemm_status, 0u, (unsigned)FP8_ERR_TIMEOUT);
+      return;
+    }
+}
+
+__device__ __forceinline__ void decode_unit(const GemmArgs &g, int64_t u, int &tm, int &tn,
+                                            int &kb0, int &kb1) {
+  const int split = (int)(u % g.splits);
+  const int64_t t = u / g.splits;
+  tm = (int)(t / g.tiles_n);
+  tn = (int)(t % g.tiles_n);
+  kb0 = split * g.kb_per_split;
+  kb1 = min(g.kbs, kb0 + g.kb_per_split);
+}
+
+// Write 32 consecutive outputs of row m starting at column col0.
+template <bool SPLIT>
+__device__ __forceinline__ void store32(const GemmArgs &g, int split, int64_t m, int64_t col0,
+                                        const float (&v)[32]) {
+  if (m >= g.M) return;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const int64_t n = col0 + 8 * p;
+    if (n >= g.N) continue;
+    if (SPLIT) {
+      float *dst = static_cast<float *>(g.out) + ((int64_t)split * g.M + m) * g.N + n;
+      reinterpret_cast<float4 *>(dst)[0] = make_float4(v[8 * p], v[8 * p + 1], v[8 * p + 2], v[8 * p + 3]);
+      reinterpret_cast<float4 *>(dst)[1] = make_float4(v[8 * p + 4], v[8 * p + 5], v[8 * p + 6], v[8 * p + 7]);
+    } else {
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * p + 2 * j], v[8 * p + 2 * j + 1]);
+        w[j] = *reinterpret_cast<uint32_t *>(&b);
+      }
+      __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(g.out) + m * g.N + n;
+      *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+template <int SCALING, bool SPLIT>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const GemmArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  SmemCtl *ctl = reinterpret_cast<SmemCtl *>(smem + (size_t)kStages * kStageBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&ctl->full[s], 1);
+      ptx::mbar_init(&ctl->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&ctl->acc_full[b], 1);
+      ptx::mbar_init(&ctl->acc_empty[b], kEpiWarps);
+    }
+    ptx::mbar_init(&ctl->mma_done, 1);
+    ctl->abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&ctl->tmem_base, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  volatile int *abort = &ctl->abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int last_phase[kStages];
+      for (int s = 0; s < kStages; ++s) last_phase[s] = -1;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
+        int tm, tn, kb0, kb1;
+        decode_unit(g, u, tm, tn, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait_bar(&ctl->empty[stage], phase ^ 1, abort)) { ok = false; break; }
+          uint8_t *sa = smem + (size_t)stage * kStageBytes;
+          ptx::mbar_arrive_expect_tx(&ctl->full[stage], kStageBytes);
+          ptx::tma_load_2d(sa, &tmA, &ctl->full[stage], kb * BK, tm * BM);
+          ptx::tma_load_2d(sa + kStageA, &tmB, &ctl->full[stage], kb * BK, tn * BN);
+          last_phase[stage] = (int)phase;
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok)  // let every issued copy land before the CTA can exit
+        for (int s = 0; s < kStages; ++s)
+          if (last_phase[s] >= 0) drain_wait(&ctl->full[s], (uint32_t)last_phase[s]);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t nacc = 0;  // accumulator-buffer uses so far
+      bool ok = true;
+      for (int64_t u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
+        int tm, tn, kb0, kb1;
+        decode_unit(g, u, tm, tn, kb0, kb1);
+        if (SCALING == FP8_SCALING_TENSOR) {
+          const uint32_t ab = nacc & 1, aph = (nacc >> 1) & 1;
+          if (!wait_bar(&ctl->acc_empty[ab], aph ^ 1, abort)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t d = tmem + ab * BN;
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!wait_bar(&ctl->full[stage], phase, abort)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t a_addr = ptx::smem_u32(smem + (size_t)stage * kStageBytes);
+            const uint64_t adesc = ptx::smem_desc_sw128(a_addr);
+            const uint64_t bdesc = ptx::smem_desc_sw128(a_addr + kStageA);
+#pragma unroll
+            for (int k = 0; k < BK / 32; ++k)
+              ptx::mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, g.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            ptx::mma_commit(&ctl->empty[stage]);
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
+          }
+          if (!ok) break;
+          ptx::mma_commit(&ctl->acc_full[ab]);
+          ++nacc;
+        } else {
+          for (int kb = kb0; kb < kb1; ++kb) {
+            const uint32_t ab = nacc & 1, aph = (nacc >> 1) & 1;
+            if (!wait_bar(&ctl->acc_empty[ab], aph ^ 1, abort)) { ok = false; break; }
+            ptx::tc_fence_after();
+            if (!wait_bar(&ctl->full[stage], phase, abort)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t d = tmem + ab * BN;
+            const uint32_t a_addr = ptx::smem_u32(smem + (size_t)stage * kStageBytes);
+            const uint64_t adesc = ptx::smem_desc_sw128(a_addr);
+            const uint64_t bdesc = ptx::smem_desc_sw128(a_addr + kStageA);
+#pragma unroll
+            for (int k = 0; k < BK / 32; ++k)
+              ptx::mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, g.idesc, k > 0 ? 1u : 0u);
+            ptx::mma_commit(&ctl->empty[stage]);
+            ptx::mma_commit(&ctl->acc_full[ab]);
+            ++nacc;
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
+          }
+        }
+      }
+      // all issued MMAs complete before TMEM is freed / the CTA exits
+      ptx::mma_commit(&ctl->mma_done);
+      drain_wait(&ctl->mma_done, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;          // TMEM lane quarter this warp may access
+    const int h = (warp - 2) >> 2;   // column half of the tile
+    const int r = q * 32 + lane;     // tile row owned by this thread
+    const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 64);
+    uint32_t nacc = 0;
+    float s_tensor = 0.0f;
+    if (SCALING == FP8_SCALING_TENSOR) s_tensor = __fmul_rn(g.a_sinv[0], g.b_sinv[0]);
+    for (int64_t u = blockIdx.x; u < g.units; u += gridDim.x) {
+      int tm, tn, kb0, kb1;
+      decode_unit(g, u, tm, tn, kb0, kb1);
+      const int split = (int)(u % g.splits);
+      const int64_t m = (int64_t)tm * BM + r;
+      const int64_t colbase = (int64_t)tn * BN + h * 64;
+      bool ok = true;
+      if (SCALING == FP8_SCALING_TENSOR) {
+        const uint32_t ab = nacc & 1, aph = (nacc >> 1) & 1;
+        if (!wait_bar(&ctl->acc_full[ab], aph, abort)) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t raw[32];
+          ptx::tmem_ld32(tl + ab * BN + 32 * c, raw);
+          ptx::tmem_ld_wait();
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(raw[j]), s_tensor);
+          store32<SPLIT>(g, split, m, colbase + 32 * c, v);
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty[ab]);
+        ++nacc;
+      } else {
+        float acc[64];
+#pragma unroll
+        for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+        const int64_t mrow = m < g.M ? m : g.M - 1;  // clamp for the scale read only
+        for (int kb = kb0; kb < kb1; ++kb) {
+          const uint32_t ab = nacc & 1, aph = (nacc >> 1) & 1;
+          const float sa = g.a_sinv[mrow * g.lds_a + kb];
+          float sb_tile = 0.0f;
+          if (SCALING == FP8_SCALING_1x128_128x128) {
+            sb_tile = g.b_sinv[(int64_t)tn * g.lds_b + kb];
+          } else {
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const int64_t n = colbase + 32 * c + lane;
+              ctl->bscale[warp - 2][32 * c + lane] =
+                  n < g.N ? g.b_sinv[n * g.lds_b + kb] : 0.0f;
+            }
+            __syncwarp();
+          }
+          if (!wait_bar(&ctl->acc_full[ab], aph, abort)) { ok = false; break; }
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t raw[32];
+            ptx::tmem_ld32(tl + ab * BN + 32 * c, raw);
+            ptx::tmem_ld_wait();
+            if (SCALING == FP8_SCALING_1x128_128x128) {
+              const float s = __fmul_rn(sa, sb_tile);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(__uint_as_float(raw[j]), s, acc[32 * c + j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float s = __fmul_rn(sa, ctl->bscale[warp - 2][32 * c + j]);
+                acc[32 * c + j] = fmaf(__uint_as_float(raw[j]), s, acc[32 * c + j]);
+              }
+            }
+          }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty[ab]);
+          ++nacc;
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = acc[32 * c + j];
+          store32<SPLIT>(g, split, m, colbase + 32 * c, v);
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Fixed-order sum of the split-K partials, rounded once to bf16.
+__global__ void splitk_reduce_kernel(const float *__restrict__ ws, int splits, int64_t mn,
+                                     __nv_bfloat16 *__restrict__ C) {
+  const int64_t n4 = mn / 4;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float4 a = reinterpret_cast<const float4 *>(ws)[i];
+    for (int s = 1; s < splits; ++s) {
+      const float4 b = reinterpret_cast<const float4 *>(ws + (int64_t)s * mn)[i];
+      a.x = __fadd_rn(a.x, b.x);
+      a.y = __fadd_rn(a.y, b.y);
+      a.z = __fadd_rn(a.z, b.z);
+      a.w = __fadd_rn(a.w, b.w);
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
+    uint2 w;
+    w.x = *reinterpret_cast<uint32_t *>(&lo);
+    w.y = *reinterpret_cast<uint32_t *>(&hi);
+    reinterpret_cast<uint2 *>(C)[i] = w;
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// [rows, cols] u8 row-major, boxes of 128 rows x 128 bytes, 128-byte swizzle,
+// zero fill outside the tensor.
+bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Plan {
+  int tiles_m, tiles_n, kbs, splits, kb_per_split;
+};
+
+Plan make_plan(int64_t M, int64_t N, int64_t K) {
+  Plan p;
+  p.tiles_m = (int)((M + BM - 1) / BM);
+  p.tiles_n = (int)((N + BN - 1) / BN);
+  p.kbs = (int)((K + BK - 1) / BK);
+  const int64_t tiles = (int64_t)p.tiles_m * p.tiles_n;
+  int s = 1;
+  if (tiles < kSplitTargetCtas) {
+    s = (int)(kSplitTargetCtas / tiles);
+    s = std::min(s, std::max(1, p.kbs / 4));  // at least 4 K blocks per split
+    s = std::min(s, 32);
+    s = std::max(s, 1);
+  }
+  p.kb_per_split = (p.kbs + s - 1) / s;
+  p.splits = (p.kbs + p.kb_per_split - 1) / p.kb_per_split;
+  return p;
+}
+
+template <int SCALING, bool SPLIT>
+cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g,
+                           cudaStream_t st) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(fp8_gemm_kernel<SCALING, SPLIT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  static const char *names[3] = {"gemm_fp8_tensor", "gemm_fp8_block_1x128_128x128",
+                                 "gemm_fp8_block_1x128_1x128"};
+  const int64_t grid = std::min<int64_t>(g.units, num_sms());
+  // algorithmic bytes: FP8 operands once, bf16 output once, block scales
+  double bytes = (double)g.M * g.K + (double)g.N * g.K + 2.0 * g.M * g.N;
+  if (SCALING == FP8_SCALING_1x128_128x128) bytes += 4.0 * g.kbs * (g.M + g.tiles_n);
+  if (SCALING == FP8_SCALING_1x128_1x128) bytes += 4.0 * g.kbs * (g.M + g.N);
+  LaunchScope ls(names[SCALING], st, bytes, 2.0 * g.M * g.N * g.K);
+  fp8_gemm_kernel<SCALING, SPLIT><<<(unsigned)grid, kThreads, kSmemBytes, st>>>(ta, tb, g);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int scaling) {
+  (void)scaling;
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  const Plan p = make_plan(M, N, K);
+  return p.splits > 1 ? (size_t)p.splits * (size_t)M * (size_t)N * sizeof(float) : 0;
+}
+
+cudaError_t launch_gemm(const uint8_t *A, int a_fmt, const float *a_sinv, const uint8_t *B,
+                        int b_fmt, const float *b_sinv, int64_t M, int64_t N, int64_t K,
+                        int scaling, void *C, void *ws, cudaStream_t st) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  if (K == 0) return cudaMemsetAsync(C, 0, (size_t)M * N * 2, st);
+  const Plan p = make_plan(M, N, K);
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, A, M, K) || !make_map(&tb, B, N, K)) return cudaErrorInvalidValue;
+  GemmArgs g;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.tiles_m = p.tiles_m;
+  g.tiles_n = p.tiles_n;
+  g.kbs = p.kbs;
+  g.splits = p.splits;
+  g.kb_per_split = p.kb_per_split;
+  g.units = (int64_t)p.tiles_m * p.tiles_n * p.splits;
+  g.a_sinv = a_sinv;
+  g.b_sinv = b_sinv;
+  g.lds_a = p.kbs;
+  g.lds_b = p.kbs;
+  g.out = p.splits > 1 ? ws : C;
+  g.idesc = ptx::idesc_f8f6f4((uint32_t)a_fmt, (uint32_t)b_fmt, BM, BN);
+  cudaError_t e;
+  const bool split = p.splits > 1;
+  switch (scaling) {
+    case FP8_SCALING_TENSOR:
+      e = split ? launch_variant<FP8_SCALING_TENSOR, true>(ta, tb, g, st)
+                : launch_variant<FP8_SCALING_TENSOR, false>(ta, tb, g, st);
+      break;
+    case FP8_SCALING_1x128_128x128:
+      e = split ? launch_variant<FP8_SCALING_1x128_128x128, true>(ta, tb, g, st)
+                : launch_variant<FP8_SCALING_1x128_128x128, false>(ta, tb, g, st);
+      break;
+    default:
+      e = split ? launch_variant<FP8_SCALING_1x128_1x128, true>(ta, tb, g, st)
+                : launch_variant<FP8_SCALING_1x128_1x128, false>(ta, tb, g, st);
+      break;
+  }
+  if (e != cudaSuccess || !split) return e;
+  const int64_t mn = M * N;
+  const int64_t blocks = std::min<int64_t>((mn / 4 + 255) / 256, (int64_t)num_sms() * 8);
+  LaunchScope ls("gemm_splitk_reduce", st, 4.0 * p.splits * mn + 2.0 * mn, (double)p.splits * mn);
+  splitk_reduce_kernel<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, st>>>(
+      static_cast<const float *>(ws), p.splits, mn, static_cast<__nv_bfloat16 *>(C));
+  return cudaGetLastError();
+}
+
+cudaError_t gemm_read_status(unsigned *status, cudaStream_t st) {
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbol(status, g_gemm_status, sizeof(unsigned));
+  if (e != cudaSuccess) return e;
+  const unsigned zero = 0;
+  return cudaMemcpyToSymbol(g_gemm_status, &zero, sizeof(unsigned));
+}
+
+}  // namespace fp8lin

@@ -1,0 +1,54 @@
+// Internal launcher interface between the C-ABI layer (api.cpp) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stddef.h>
+#include <algorithm>
+
+namespace fp8lin {
+
+// Host-side launch counter (defined in api.cpp).
+void count_launch();
+
+// Brackets one kernel launch with CUDA events on its stream while kernel
+// timing is enabled (fp8_profile_begin/end); also counts the launch.
+// bytes/flops: the launch's algorithmic HBM traffic and floating-point work.
+class LaunchScope {
+ public:
+  LaunchScope(const char *name, cudaStream_t st, double bytes, double flops);
+  ~LaunchScope();
+
+ private:
+  int rec_ = -1;
+  cudaStream_t st_;
+};
+
+// Tensorwise quantization keeps one fp32 partial amax per CTA of its first
+// pass in the caller's workspace; at most this many.
+constexpr int kMaxPartials = 1024;
+
+int num_sms();
+int tensorwise_partials_count(int64_t rows, int64_t cols);
+
+// mode: 0 tensorwise, 1 1x128 blocks, 2 128x128 tiles; fmt: fp8_format.
+cudaError_t launch_quantize(const void *x, int64_t rows, int64_t cols, int mode, int fmt,
+                            uint8_t *out_row, uint8_t *out_col, float *row_scale,
+                            float *row_scale_inv, float *col_scale, float *col_scale_inv,
+                            float *partials, cudaStream_t st);
+
+// FP8 GEMM (tcgen05).  scaling: fp8_scaling.  ws may be null when
+// gemm_workspace_bytes() is 0.
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int scaling);
+cudaError_t launch_gemm(const uint8_t *A, int a_fmt, const float *a_sinv, const uint8_t *B,
+                        int b_fmt, const float *b_sinv, int64_t M, int64_t N, int64_t K,
+                        int scaling, void *C, void *ws, cudaStream_t st);
+// Reads and clears the GEMM kernels' device status word (0 = ok).
+cudaError_t gemm_read_status(unsigned *status, cudaStream_t st);
+
+cudaError_t launch_gelu_fwd(const void *H, void *A, int64_t n, cudaStream_t st);
+cudaError_t launch_gelu_bwd(const void *dA, const void *H, void *dH, int64_t n, cudaStream_t st);
+cudaError_t launch_grad_accumulate(float *acc, const void *dW, int64_t n, cudaStream_t st);
+
+}  // namespace fp8lin

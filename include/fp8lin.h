@@ -1,0 +1,254 @@
+/*
+ * fp8lin.h - C ABI of the GB300 (sm_103a) FP8 linear-layer library.
+ *
+ * The library implements the FP8 linear layer of a training step:
+ *   quantizers  - fused amax -> fp32 scale -> saturating round-to-nearest-even
+ *                 cast, writing the row-major and the transposed FP8 layout in
+ *                 one pass ("Native FP8 MLP reconstruction", implementation
+ *                 paragraph: current tensorwise amax, E4M3 inputs/weights, E5M2
+ *                 incoming gradients, fused cast emitting ordinary and
+ *                 transposed layouts);
+ *   weight cache - is_first_microbatch semantics ("FP8 weight caching shows no
+ *                 speedup ... under Float8BlockScaling", TransformerEngine
+ *                 issue #2852, opening post and maintainer reply);
+ *   FP8 GEMMs   - fprop, dgrad and wgrad on tcgen05 tensor cores with fp32
+ *                 accumulation and BF16 output (use_fast_accum=False in the
+ *                 reconstruction's implementation paragraph).
+ *
+ * Conventions shared by every call
+ *   - Tensors are dense and row-major.  X is [N, K] (tokens x in features),
+ *     W is [O, K] (out x in), Y = X W^T is [N, O].  A "colwise" or
+ *     "transposed" layout of an [R, C] tensor is the [C, R] array, row-major.
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller, 16-byte
+ *     aligned.  The library allocates no device memory; scratch space is the
+ *     caller's `workspace` (size from the *_workspace_size queries).
+ *   - Every dimension must be a multiple of 16 (TMA row-stride rule).  A
+ *     dimension need not be a multiple of 128: the last 128-block of a row,
+ *     column or tile is then shorter ("ragged tail") and its amax covers the
+ *     elements present.  A zero dimension makes the call a no-op (FP8_OK).
+ *   - bf16 tensors are passed as `const void*` (IEEE bfloat16 bit patterns).
+ *   - Every call enqueues work on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and returns without synchronising, except
+ *     fp8_get_device_status.  Arguments are validated before anything is
+ *     launched: on a non-OK status nothing was enqueued.
+ *   - Calls are not thread-safe with respect to one fp8_weight_cache object.
+ *
+ * Recipes
+ *   FP8_RECIPE_TENSORWISE: one current (just-in-time) amax per tensor.
+ *   FP8_RECIPE_BLOCK (Float8BlockScaling reading): activations and gradients
+ *     use 1x128 blocks along each layout's contiguous dimension, weights use
+ *     128x128 tiles.  No amax history in either recipe.
+ *   Scale rule (both recipes): scale = fp32(fmax / amax) (IEEE division,
+ *   round-to-nearest-even), scale_inv = fp32(1 / scale); fmax = 448 (E4M3) or
+ *   57344 (E5M2).  amax == 0 gives scale = scale_inv = 1; a quotient that
+ *   overflows gives scale = FLT_MAX.  amax ignores NaN.  The cast is one fp32
+ *   multiply x * scale, then saturating round-to-nearest-even to 8 bits;
+ *   NaN encodes to 0x7F.
+ *
+ * Scale array shapes (float32, row-major), for an [R, C] input
+ *   tensorwise        : rowwise [1], colwise [1] (same value)
+ *   1x128 (act, grad) : rowwise [R, ceil(C/128)], colwise [C, ceil(R/128)]
+ *   128x128 (weight)  : rowwise [ceil(R/128), ceil(C/128)], colwise = its transpose
+ */
+#ifndef FP8LIN_H
+#define FP8LIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *fp8_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  FP8_OK = 0,
+  FP8_ERR_INVALID_ARG = 1, /* null pointer where one is required, bad enum, negative size */
+  FP8_ERR_SHAPE = 2,       /* a dimension not a multiple of 16, or inconsistent shapes */
+  FP8_ERR_ALIGN = 3,       /* a device pointer not 16-byte aligned */
+  FP8_ERR_STALE = 4,       /* weight-cache entry not quantized in this cycle, or its version changed */
+  FP8_ERR_TIMEOUT = 5,     /* a device-side wait gave up (reported by fp8_get_device_status) */
+  FP8_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed */
+  FP8_ERR_UNSUPPORTED = 7, /* request this build does not implement */
+  FP8_ERR_WORKSPACE = 8    /* workspace smaller than the size query returned */
+} fp8_status;
+
+typedef enum { FP8_RECIPE_TENSORWISE = 0, FP8_RECIPE_BLOCK = 1 } fp8_recipe;
+
+/* Operand role: ACT and WEIGHT use E4M3, GRAD uses E5M2 (reconstruction,
+ * implementation paragraph).  Under FP8_RECIPE_BLOCK, WEIGHT selects 128x128
+ * tiles and ACT/GRAD select 1x128 blocks. */
+typedef enum { FP8_ROLE_ACT = 0, FP8_ROLE_WEIGHT = 1, FP8_ROLE_GRAD = 2 } fp8_role;
+
+typedef enum { FP8_FORMAT_E4M3 = 0, FP8_FORMAT_E5M2 = 1 } fp8_format;
+
+/* Scale layouts of the two GEMM operands (see fp8_gemm). */
+typedef enum {
+  FP8_SCALING_TENSOR = 0,        /* a_scale_inv [1], b_scale_inv [1] */
+  FP8_SCALING_1x128_128x128 = 1, /* a [M, ceil(K/128)], b [ceil(N/128), ceil(K/128)] (fprop, dgrad) */
+  FP8_SCALING_1x128_1x128 = 2    /* a [M, ceil(K/128)], b [N, ceil(K/128)]          (wgrad)        */
+} fp8_scaling;
+
+/* Human-readable name of a status code (static string). */
+const char *fp8_status_string(fp8_status s);
+
+/* Number of kernels this library has launched since it was loaded (all
+ * devices, all streams).  Host-side counter, incremented once per launch. */
+uint64_t fp8_launch_count(void);
+
+/* ------------------------------------------------------------------ quantize
+ * fp8_quantize: fused amax -> scale -> cast of a bf16 [rows, cols] tensor,
+ * writing the row-major bytes `rowwise_out` [rows, cols] and/or the
+ * transposed bytes `colwise_out` [cols, rows] in one pass over the input
+ * (tensorwise: one extra read of the input for the global amax).
+ *   x              device bf16 [rows, cols]
+ *   recipe, role   select format and block shape (see above)
+ *   rowwise_out    device u8 [rows, cols] or NULL
+ *   colwise_out    device u8 [cols, rows] or NULL (not both NULL)
+ *   row_scale, row_scale_inv  device f32, rowwise scale shape; required
+ *                  when rowwise_out != NULL, and always for tensorwise
+ *   col_scale, col_scale_inv  device f32, colwise scale shape; required when
+ *                  colwise_out != NULL under 1x128 and 128x128; ignored
+ *                  (may be NULL) under tensorwise
+ *   workspace      device scratch of fp8_quantize_workspace_size bytes
+ *                  (NULL allowed when that size is 0)
+ * Errors: INVALID_ARG, SHAPE, ALIGN, WORKSPACE, CUDA.
+ */
+fp8_status fp8_quantize(const void *x, int64_t rows, int64_t cols, fp8_recipe recipe, fp8_role role,
+                        uint8_t *rowwise_out, uint8_t *colwise_out, float *row_scale,
+                        float *row_scale_inv, float *col_scale, float *col_scale_inv,
+                        void *workspace, size_t workspace_bytes, fp8_stream_t stream);
+
+fp8_status fp8_quantize_workspace_size(fp8_recipe recipe, int64_t rows, int64_t cols,
+                                       size_t *bytes);
+
+/* Shape [srows, scols] of the scale array of a layout (colwise = 0 or 1). */
+fp8_status fp8_scale_shape(fp8_recipe recipe, fp8_role role, int64_t rows, int64_t cols,
+                           int colwise, int64_t *srows, int64_t *scols);
+
+/* ------------------------------------------------------------------ GEMM
+ * fp8_gemm: C[M, N] (bf16) = sum_k (A[m, k] * sa) * (B[n, k] * sb), both
+ * operands K-major (row-major [M, K] and [N, K] bytes).  sa, sb are the
+ * scale_inv values of each element's block under `scaling`.  The tensor
+ * cores accumulate in fp32; under the block scalings every 128-deep K block
+ * is accumulated separately and added, scaled, into an fp32 accumulator.
+ * The result is rounded once to bf16 (round-to-nearest-even).
+ *   a_fmt, b_fmt   FP8 format of each operand (E4M3 or E5M2, may differ)
+ *   workspace      device scratch, fp8_gemm_workspace_size bytes (split-K
+ *                  partial sums; 0 when no split is used)
+ * Deterministic: the kernel configuration, split and summation order are a
+ * function of (M, N, K, scaling) only.
+ * Errors: INVALID_ARG, SHAPE, ALIGN, WORKSPACE, CUDA.
+ */
+fp8_status fp8_gemm(const uint8_t *A, fp8_format a_fmt, const float *a_scale_inv,
+                    const uint8_t *B, fp8_format b_fmt, const float *b_scale_inv, int64_t M,
+                    int64_t N, int64_t K, fp8_scaling scaling, void *C, void *workspace,
+                    size_t workspace_bytes, fp8_stream_t stream);
+
+fp8_status fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, fp8_scaling scaling,
+                                   size_t *bytes);
+
+/* ------------------------------------------------------------------ weight cache
+ * is_first_microbatch semantics (TransformerEngine issue #2852, opening post;
+ * maintainer reply: under non-delayed recipes cached and uncached runs are
+ * exactly equal and caching saves the weight re-quantization).
+ *   begin_cycle  = start of a gradient-accumulation cycle: every entry becomes
+ *                  stale, so the next get() with use_cache re-quantizes
+ *                  (is_first_microbatch=True);
+ *   get(use_cache=1) on a fresh entry reuses the FP8 copy
+ *                  (is_first_microbatch=False);
+ *   get(use_cache=0) always re-quantizes (is_first_microbatch=None).
+ * The cache is a host object; the FP8 buffers it fills are caller-owned
+ * device memory registered once per weight.
+ */
+typedef struct fp8_weight_cache fp8_weight_cache;
+typedef int32_t fp8_weight_handle;
+
+fp8_status fp8_weight_cache_create(fp8_weight_cache **out);
+void fp8_weight_cache_destroy(fp8_weight_cache *cache);
+
+/* Register the bf16 weight W [O, K] and the caller-owned buffers that will
+ * hold its FP8 copy: w_row [O, K], w_col [K, O] and their scale arrays
+ * (weight role shapes under `recipe`).  `workspace` (size from
+ * fp8_quantize_workspace_size(recipe, O, K)) must stay valid for every get()
+ * of this handle.  Errors: INVALID_ARG, SHAPE, ALIGN, WORKSPACE. */
+fp8_status fp8_weight_cache_register(fp8_weight_cache *cache, const void *w, int64_t O,
+                                     int64_t K, fp8_recipe recipe, uint8_t *w_row,
+                                     uint8_t *w_col, float *row_scale, float *row_scale_inv,
+                                     float *col_scale, float *col_scale_inv, void *workspace,
+                                     size_t workspace_bytes, fp8_weight_handle *out);
+
+fp8_status fp8_weight_cache_begin_cycle(fp8_weight_cache *cache);
+
+/* Make the FP8 copy of weight `h` current on `stream`.  w_version is a
+ * caller-maintained counter of the bf16 weight's contents: get() with
+ * use_cache on an entry already quantized in this cycle under another
+ * version returns FP8_ERR_STALE (the weight changed mid-cycle).
+ * *requantized (optional) is set to 1 when a quantization was enqueued. */
+fp8_status fp8_weight_cache_get(fp8_weight_cache *cache, fp8_weight_handle h, uint64_t w_version,
+                                int use_cache, fp8_stream_t stream, int *requantized);
+
+/* ------------------------------------------------------------------ linear layer
+ * fp8_linear_fwd: Y[N, O] = X W^T with X quantized (E4M3, both layouts) and
+ * the cached FP8 weight; writes Y (bf16) and the context the backward needs
+ * (the transposed FP8 X and its scales) into `ctx`.
+ * fp8_linear_bwd: dY[N, O] is quantized separately (E5M2, both layouts);
+ * dX[N, K] = dY W (dgrad, forward-rounded W reused; dX may be NULL) and
+ * dW[O, K] = dY^T X (wgrad, forward-rounded X from ctx reused).  Scales are
+ * constants of the backward (detached).
+ * The weight handle must have been made current by fp8_weight_cache_get in
+ * the current cycle (else FP8_ERR_STALE) and `recipe` must equal its
+ * registered recipe (else FP8_ERR_INVALID_ARG).
+ *   ctx  device buffer of fp8_linear_ctx_size bytes, written by fwd, read by bwd
+ *   ws   device scratch of fp8_linear_workspace_size bytes (shared by fwd and bwd)
+ */
+fp8_status fp8_linear_ctx_size(fp8_recipe recipe, int64_t N, int64_t K, size_t *bytes);
+fp8_status fp8_linear_workspace_size(fp8_recipe recipe, int64_t N, int64_t K, int64_t O,
+                                     size_t *bytes);
+fp8_status fp8_linear_fwd(const void *X, int64_t N, int64_t K, fp8_weight_cache *cache,
+                          fp8_weight_handle h, fp8_recipe recipe, void *Y, void *ctx, void *ws,
+                          size_t ws_bytes, fp8_stream_t stream);
+fp8_status fp8_linear_bwd(const void *dY, int64_t N, int64_t O, const void *ctx,
+                          fp8_weight_cache *cache, fp8_weight_handle h, fp8_recipe recipe,
+                          void *dX, void *dW, void *ws, size_t ws_bytes, fp8_stream_t stream);
+
+/* ------------------------------------------------------------------ MLP glue
+ * GELU in its exact erf form, fp32 arithmetic, bf16 in/out, n elements
+ * (n a multiple of 8): A = H * Phi(H); dH = dA * (Phi(H) + H * phi(H)).
+ * fp8_grad_accumulate: acc[i] += float(dW[i]) in fp32 (one add per element),
+ * for gradient accumulation over microbatches. */
+fp8_status fp8_gelu_fwd(const void *H, void *A, int64_t n, fp8_stream_t stream);
+fp8_status fp8_gelu_bwd(const void *dA, const void *H, void *dH, int64_t n, fp8_stream_t stream);
+fp8_status fp8_grad_accumulate(float *acc, const void *dW, int64_t n, fp8_stream_t stream);
+
+/* ------------------------------------------------------------------ kernel timing
+ * Per-kernel timing for roofline reports.  Between fp8_profile_begin and
+ * fp8_profile_end every kernel this library launches is bracketed by two
+ * CUDA events recorded on its own launch stream, and the launcher's
+ * algorithmic byte and flop counts for that launch are recorded with it.
+ * fp8_profile_end synchronises those events and returns one record per
+ * kernel name (at most `cap`; *n receives the number of distinct names).
+ * Not thread-safe; host-side bookkeeping only. */
+typedef struct {
+  char name[64];
+  uint64_t launches;
+  double total_ms;   /* sum of event-measured durations */
+  double bytes;      /* sum of algorithmic HBM bytes (reads + writes) */
+  double flops;      /* sum of algorithmic floating-point operations */
+} fp8_kernel_stat;
+
+fp8_status fp8_profile_begin(void);
+fp8_status fp8_profile_end(fp8_kernel_stat *out, int cap, int *n);
+
+/* ------------------------------------------------------------------ device status
+ * Synchronises `stream`, then returns and clears the device-side status word
+ * that kernels set when a bounded wait gives up (FP8_ERR_TIMEOUT) - no kernel
+ * traps.  Also returns FP8_ERR_CUDA if the stream reports an error. */
+fp8_status fp8_get_device_status(fp8_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8LIN_H */

@@ -44,7 +44,7 @@ FP8 tensors as uint8 bytes, scales as float32.
 from __future__ import annotations
 
 import numpy as np
-from scipy.special import erf as _erf
+from scipy.special import erfc as _erfc
 
 # ---------------------------------------------------------------------------
 # FP8 formats  ([NFP8] implementation paragraph names E4M3 and E5M2; the bit
@@ -223,44 +223,58 @@ def quantize_tensorwise(x_bits: np.ndarray, fmt: str) -> dict:
                 col_scale=s1.copy(), col_scale_inv=si1.copy(), amax=amax)
 
 
+def _pad128(xf: np.ndarray) -> np.ndarray:
+    """Zero-pad both dimensions up to multiples of 128.  Zeros never raise an
+    amax, so a ragged tail block's amax covers exactly the elements present;
+    padded outputs are cropped away."""
+    R, C = xf.shape
+    Rp, Cp = -(-R // 128) * 128, -(-C // 128) * 128
+    if (Rp, Cp) == (R, C):
+        return xf
+    out = np.zeros((Rp, Cp), dtype=xf.dtype)
+    out[:R, :C] = xf
+    return out
+
+
 def quantize_1x128(x_bits: np.ndarray, fmt: str) -> dict:
     """1x128 block scaling for activations and gradients.
 
-    Rowwise: each row's 128-column slices are blocks; scales [R, C/128].
+    Rowwise: each row's 128-column slices are blocks; scales [R, ceil(C/128)].
     Colwise: each column's 128-row slices are blocks; the bytes are stored
-    transposed, [C, R], with scales [C, R/128].
+    transposed, [C, R], with scales [C, ceil(R/128)].
     """
     R, C = x_bits.shape
-    assert R % 128 == 0 and C % 128 == 0
-    xf = bf16_to_f32(x_bits)
+    xf = _pad128(bf16_to_f32(x_bits))
+    Rp, Cp = xf.shape
     # rowwise blocks: x[i, 128b : 128b+128]
-    xr = xf.reshape(R, C // 128, 128)
-    amax_r = amax_of(xr, axis=2)                       # [R, C/128]
+    xr = xf.reshape(Rp, Cp // 128, 128)
+    amax_r = amax_of(xr, axis=2)                       # [Rp, Cp/128]
     s_r, si_r = scale_from_amax(amax_r, fmt)
-    q_row = cast(xr, s_r[:, :, None], fmt).reshape(R, C)
+    q_row = cast(xr, s_r[:, :, None], fmt).reshape(Rp, Cp)[:R, :C]
     # colwise blocks: x[128b : 128b+128, j]
-    xc = xf.reshape(R // 128, 128, C)
-    amax_c = amax_of(xc, axis=1)                       # [R/128, C]
+    xc = xf.reshape(Rp // 128, 128, Cp)
+    amax_c = amax_of(xc, axis=1)                       # [Rp/128, Cp]
     s_c, si_c = scale_from_amax(amax_c, fmt)
-    q_c = cast(xc, s_c[:, None, :], fmt).reshape(R, C)
-    return dict(row=q_row, col=np.ascontiguousarray(q_c.T),
-                row_scale=s_r, row_scale_inv=si_r,
-                col_scale=np.ascontiguousarray(s_c.T), col_scale_inv=np.ascontiguousarray(si_c.T))
+    q_c = cast(xc, s_c[:, None, :], fmt).reshape(Rp, Cp)[:R, :C]
+    return dict(row=np.ascontiguousarray(q_row), col=np.ascontiguousarray(q_c.T),
+                row_scale=np.ascontiguousarray(s_r[:R]), row_scale_inv=np.ascontiguousarray(si_r[:R]),
+                col_scale=np.ascontiguousarray(s_c.T[:C]), col_scale_inv=np.ascontiguousarray(si_c.T[:C]))
 
 
 def quantize_128x128(x_bits: np.ndarray, fmt: str) -> dict:
     """128x128 block scaling for weights: one scale per 128x128 tile, scales
-    [R/128, C/128]; the transposed layout is the byte transpose with the
-    transposed scale grid."""
+    [ceil(R/128), ceil(C/128)]; the transposed layout is the byte transpose
+    with the transposed scale grid."""
     R, C = x_bits.shape
-    assert R % 128 == 0 and C % 128 == 0
-    xf = bf16_to_f32(x_bits)
-    xt = xf.reshape(R // 128, 128, C // 128, 128)
-    amax_t = amax_of(xt, axis=(1, 3))                  # [R/128, C/128]
+    xf = _pad128(bf16_to_f32(x_bits))
+    Rp, Cp = xf.shape
+    xt = xf.reshape(Rp // 128, 128, Cp // 128, 128)
+    amax_t = amax_of(xt, axis=(1, 3))                  # [Rp/128, Cp/128]
     s, si = scale_from_amax(amax_t, fmt)
-    q = cast(xt, s[:, None, :, None], fmt).reshape(R, C)
-    return dict(row=q, col=np.ascontiguousarray(q.T), row_scale=s, row_scale_inv=si,
-                col_scale=np.ascontiguousarray(s.T), col_scale_inv=np.ascontiguousarray(si.T))
+    q = cast(xt, s[:, None, :, None], fmt).reshape(Rp, Cp)[:R, :C]
+    return dict(row=np.ascontiguousarray(q), col=np.ascontiguousarray(q.T), row_scale=s,
+                row_scale_inv=si, col_scale=np.ascontiguousarray(s.T),
+                col_scale_inv=np.ascontiguousarray(si.T))
 
 
 def quantize(x_bits: np.ndarray, recipe: str, role: str) -> dict:
@@ -278,15 +292,17 @@ def quantize(x_bits: np.ndarray, recipe: str, role: str) -> dict:
 # ---------------------------------------------------------------------------
 def expand_scale(s_inv: np.ndarray, rows: int, cols: int) -> np.ndarray:
     """Per-element fp64 scale_inv for a [rows, cols] operand whose scale array
-    is [1] (tensorwise), [rows, cols/128] (1x128) or [rows/128, cols/128]
-    (128x128)."""
+    is [1] (tensorwise), [rows, ceil(cols/128)] (1x128 blocks along cols) or
+    [ceil(rows/128), ceil(cols/128)] (128x128 tiles)."""
     s = np.asarray(s_inv, dtype=np.float64)
+    nb_c = -(-cols // 128)
+    nb_r = -(-rows // 128)
     if s.size == 1:
         return np.full((rows, cols), float(s.reshape(-1)[0]))
-    if s.shape == (rows, cols // 128):
-        return np.repeat(s, 128, axis=1)
-    if s.shape == (rows // 128, cols // 128):
-        return np.repeat(np.repeat(s, 128, axis=0), 128, axis=1)
+    if s.shape == (rows, nb_c):
+        return np.repeat(s, 128, axis=1)[:, :cols]
+    if s.shape == (nb_r, nb_c):
+        return np.repeat(np.repeat(s, 128, axis=0), 128, axis=1)[:rows, :cols]
     raise ValueError(f"scale shape {s.shape} for operand {rows}x{cols}")
 
 
@@ -367,18 +383,23 @@ class WeightCache:
 # ---------------------------------------------------------------------------
 # MLP glue: GELU (exact erf form) and gradient accumulation
 # ---------------------------------------------------------------------------
+def _normal_cdf(h: np.ndarray) -> np.ndarray:
+    """Phi(h) = erfc(-h / sqrt(2)) / 2.  The erfc form keeps full relative
+    precision for negative h, where 1 + erf(h / sqrt(2)) would cancel."""
+    return 0.5 * _erfc(-np.asarray(h, dtype=np.float64) / np.sqrt(2.0))
+
+
 def gelu_f64(h: np.ndarray) -> np.ndarray:
     """GELU(h) = h * Phi(h), Phi the standard normal CDF."""
     h = np.asarray(h, dtype=np.float64)
-    return 0.5 * h * (1.0 + _erf(h / np.sqrt(2.0)))
+    return h * _normal_cdf(h)
 
 
 def gelu_grad_f64(h: np.ndarray) -> np.ndarray:
     """d GELU / dh = Phi(h) + h * phi(h)."""
     h = np.asarray(h, dtype=np.float64)
-    cdf = 0.5 * (1.0 + _erf(h / np.sqrt(2.0)))
     pdf = np.exp(-0.5 * h * h) / np.sqrt(2.0 * np.pi)
-    return cdf + h * pdf
+    return _normal_cdf(h) + h * pdf
 
 
 def gelu_fwd(h_bits: np.ndarray) -> np.ndarray:

@@ -1,0 +1,121 @@
+"""GPU parity of the FP8 linear layer (fwd + bwd through the C ABI) and of
+the weight cache: quantized X/W/dY bytes and scales bit-exact, Y/dX/dW within
+the GEMM tolerance, cached vs uncached outputs bitwise identical."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as o
+from fp8_mixed_precision_gb300 import synthetic as syn
+from parity import assert_bytes_equal, assert_f32_equal, check_gemm, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fp():
+    from fp8_mixed_precision_gb300 import build
+    build.build()
+    import fp8_mixed_precision_gb300 as fp
+    return fp
+
+
+def _gemm_ref(aq, asi, af, bq, bsi, bf):
+    A = o.dequantize(aq, asi, af)
+    B = o.dequantize(bq, bsi, bf)
+    return A @ B.T, np.abs(A) @ np.abs(B).T
+
+
+@pytest.mark.parametrize("recipe", ["tensorwise", "block"])
+@pytest.mark.parametrize("N,K,O", [(2048, 512, 512), (400, 272, 144), (1024, 512, 2048)])
+def test_linear_parity(fp, recipe, N, K, O):
+    x, w, dy = syn.linear_inputs(N, K, O, device="cuda")
+    cache = fp.WeightCache()
+    h = cache.register(w, recipe)
+    cache.begin_cycle()
+    assert cache.get(h, 0, True)
+    y, ctx = fp.fp8_linear_fwd(x, cache, h, recipe)
+    dx, dw = fp.fp8_linear_bwd(dy, ctx, cache, h, recipe)
+    torch.cuda.synchronize()
+    assert fp.fp8_get_device_status() == 0
+    r = o.linear_fwd_bwd(syn.bits(x), syn.bits(w), syn.bits(dy), recipe)
+    e = cache.entries[h]
+    assert_bytes_equal(e.row, r["wq"]["row"], "Wq row")
+    assert_bytes_equal(e.col, r["wq"]["col"], "Wq col")
+    assert_f32_equal(e.row_scale_inv, r["wq"]["row_scale_inv"], "W scale_inv")
+    xq, gq, wq = r["xq"], r["gq"], r["wq"]
+    ref, ab = _gemm_ref(xq["row"], xq["row_scale_inv"], "e4m3", wq["row"], wq["row_scale_inv"], "e4m3")
+    check_gemm(y, ref, ab, K, "Y")
+    ref, ab = _gemm_ref(gq["row"], gq["row_scale_inv"], "e5m2", wq["col"], wq["col_scale_inv"], "e4m3")
+    check_gemm(dx, ref, ab, O, "dX")
+    ref, ab = _gemm_ref(gq["col"], gq["col_scale_inv"], "e5m2", xq["col"], xq["col_scale_inv"], "e4m3")
+    check_gemm(dw, ref, ab, N, "dW")
+
+
+@pytest.mark.parametrize("recipe", ["block", "tensorwise"])
+def test_weight_cache_bitwise_and_launches(fp, recipe):
+    """GA=4 microbatches, 2 cycles: is_first_microbatch True/False vs None give
+    bitwise identical outputs and gradients; the cached run quantizes each
+    weight once per cycle."""
+    N, K, O = 1024, 512, 1024
+    w = syn.bf16_normal((O, K), 0.02, 43, device="cuda")
+    xs = [syn.bf16_normal((N, K), 1.0, 100 + i, device="cuda") for i in range(4)]
+    dys = [syn.bf16_normal((N, O), 1e-3, 200 + i, device="cuda") for i in range(4)]
+    outs = {}
+    for use in (False, True):
+        cache = fp.WeightCache()
+        h = cache.register(w, recipe)
+        ws = fp.linear_workspace(recipe, N, K, O, "cuda")
+        res, nq = [], 0
+        for cycle in range(2):
+            cache.begin_cycle()
+            for mb in range(4):
+                nq += cache.get(h, cycle, use)
+                y, ctx = fp.fp8_linear_fwd(xs[mb], cache, h, recipe, ws=ws)
+                dx, dw = fp.fp8_linear_bwd(dys[mb], ctx, cache, h, recipe, ws=ws)
+                res.append((y.clone(), dx.clone(), dw.clone()))
+        torch.cuda.synchronize()
+        outs[use] = (res, nq)
+    assert outs[False][1] == 8 and outs[True][1] == 2
+    for a, b in zip(outs[False][0], outs[True][0]):
+        for t1, t2 in zip(a, b):
+            assert torch.equal(t1.view(torch.int16), t2.view(torch.int16))
+
+
+def test_weight_cache_stale_version(fp):
+    w = syn.bf16_normal((256, 256), 0.02, 1, device="cuda")
+    cache = fp.WeightCache()
+    h = cache.register(w, "block")
+    cache.begin_cycle()
+    assert cache.get(h, 7, True) is True
+    assert cache.get(h, 7, True) is False
+    with pytest.raises(fp.FP8Error) as ei:
+        cache.get(h, 8, True)
+    assert ei.value.status == 4
+    cache.begin_cycle()
+    assert cache.get(h, 8, True) is True
+    assert cache.get(h, 8, False) is True   # is_first_microbatch=None always re-quantizes
+
+
+def test_gelu_and_accumulate(fp):
+    hb = syn.bits(syn.bf16_normal((512, 256), 2.0, 11))
+    hb[0, :6] = [0x0000, 0x8000, 0x4120, 0xC120, 0x3F80, 0xBF80]   # 0, -0, 10, -10, 1, -1
+    h = syn.from_bits(hb, "cuda")
+    a = fp.fp8_gelu_fwd(h)
+    dab = syn.bits(syn.bf16_normal((512, 256), 1e-3, 12))
+    da = syn.from_bits(dab, "cuda")
+    dh = fp.fp8_gelu_bwd(da, h)
+    torch.cuda.synchronize()
+    for got, exp in ((a, o.gelu_fwd(hb)), (dh, o.gelu_bwd(dab, hb))):
+        g = o.bf16_to_f32(to_np(got)).astype(np.float64)
+        e = o.bf16_to_f32(exp).astype(np.float64)
+        ulp = np.ldexp(1.0, (np.maximum(np.frexp(np.abs(e))[1] - 1, -126) - 7).astype(np.int32))
+        assert np.all(np.abs(g - e) <= ulp), "GELU beyond 1 bf16 ulp"
+    acc = torch.zeros((512, 256), dtype=torch.float32, device="cuda")
+    exp = np.zeros((512, 256), np.float32)
+    for i in range(3):
+        db = syn.bits(syn.bf16_normal((512, 256), 1e-3, 30 + i))
+        fp.fp8_grad_accumulate(acc, syn.from_bits(db, "cuda"))
+        exp = o.grad_accumulate(exp, db)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(acc).view(np.uint32), exp.view(np.uint32))

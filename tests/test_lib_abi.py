@@ -1,0 +1,104 @@
+"""CPU-side checks of the C ABI: the library builds, loads and exports every
+function include/fp8lin.h declares; argument validation and the weight-cache
+bookkeeping answer without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from fp8_mixed_precision_gb300 import build
+    build.build()
+    import fp8_mixed_precision_gb300 as fp
+    return fp.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "fp8lin.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert len(names) >= 20, names
+    for n in names:
+        assert hasattr(L, n), f"missing export {n}"
+
+
+def test_status_strings(L):
+    for s in range(9):
+        assert L.fp8_status_string(s)
+    assert L.fp8_status_string(2).decode().startswith("unsupported shape")
+
+
+def test_scale_shapes(L):
+    import fp8_mixed_precision_gb300 as fp
+    assert fp.fp8_scale_shape("tensorwise", "act", 256, 512, False) == (1, 1)
+    assert fp.fp8_scale_shape("block", "act", 256, 400, False) == (256, 4)
+    assert fp.fp8_scale_shape("block", "act", 256, 400, True) == (400, 2)
+    assert fp.fp8_scale_shape("block", "weight", 256, 400, False) == (2, 4)
+    assert fp.fp8_scale_shape("block", "weight", 256, 400, True) == (4, 2)
+
+
+def test_validation_without_gpu(L):
+    P = ctypes.c_void_p
+    fake = P(4096)           # never dereferenced: every call below fails validation first
+    odd = P(4096 + 8)
+    sz = ctypes.c_size_t
+    # ragged beyond the 16-element rule
+    assert L.fp8_quantize(fake, 100, 128, 0, 0, fake, fake, fake, fake, fake, fake, fake, 4096,
+                          None) == 2
+    # bad enums
+    assert L.fp8_quantize(fake, 128, 128, 7, 0, fake, fake, fake, fake, fake, fake, fake, 4096,
+                          None) == 1
+    # misaligned pointer
+    assert L.fp8_quantize(odd, 128, 128, 1, 0, fake, fake, fake, fake, fake, fake, None, 0,
+                          None) == 3
+    # tensorwise needs its partials workspace
+    assert L.fp8_quantize(fake, 128, 128, 0, 0, fake, fake, fake, fake, fake, fake, fake, 16,
+                          None) == 8
+    # empty tensor: no-op
+    assert L.fp8_quantize(None, 0, 128, 0, 0, fake, None, None, None, None, None, None, 0,
+                          None) == 0
+    b = sz()
+    assert L.fp8_quantize_workspace_size(0, 256, 256, ctypes.byref(b)) == 0 and b.value == 4096
+    assert L.fp8_quantize_workspace_size(1, 256, 256, ctypes.byref(b)) == 0 and b.value == 0
+    assert L.fp8_gemm(fake, 0, fake, fake, 0, fake, 128, 120, 128, 0, fake, None, 0, None) == 2
+    assert L.fp8_gemm(fake, 3, fake, fake, 0, fake, 128, 128, 128, 0, fake, None, 0, None) == 1
+    # split-K GEMMs need a workspace
+    assert L.fp8_gemm_workspace_size(512, 512, 131072, 0, ctypes.byref(b)) == 0 and b.value > 0
+    assert L.fp8_gemm(fake, 0, fake, fake, 0, fake, 512, 512, 131072, 0, fake, None, 0, None) == 8
+    assert L.fp8_gemm_workspace_size(131072, 512, 512, 0, ctypes.byref(b)) == 0 and b.value == 0
+
+
+def test_weight_cache_bookkeeping_without_gpu(L):
+    P = ctypes.c_void_p
+    fake = P(4096)
+    c = P()
+    assert L.fp8_weight_cache_create(ctypes.byref(c)) == 0
+    h = ctypes.c_int32()
+    assert L.fp8_weight_cache_register(c, fake, 256, 128, 1, fake, fake, fake, fake, fake, fake,
+                                       None, 0, ctypes.byref(h)) == 0
+    assert h.value == 0
+    assert L.fp8_weight_cache_register(c, fake, 250, 128, 1, fake, fake, fake, fake, fake, fake,
+                                       None, 0, ctypes.byref(h)) == 2
+    # tensorwise weights need the partials workspace at registration
+    assert L.fp8_weight_cache_register(c, fake, 256, 128, 0, fake, fake, fake, fake, fake, fake,
+                                       None, 0, ctypes.byref(h)) == 8
+    # forward before any get() in this cycle: stale, nothing launched
+    n0 = L.fp8_launch_count()
+    assert L.fp8_linear_fwd(fake, 128, 128, c, 0, 1, fake, fake, fake, 1 << 30, None) == 4
+    # wrong recipe / wrong K for the handle
+    assert L.fp8_linear_fwd(fake, 128, 128, c, 0, 0, fake, fake, fake, 1 << 30, None) == 1
+    assert L.fp8_linear_fwd(fake, 128, 256, c, 0, 1, fake, fake, fake, 1 << 30, None) == 1
+    assert L.fp8_linear_bwd(fake, 128, 256, fake, c, 0, 1, None, fake, fake, 1 << 30, None) == 4
+    assert L.fp8_weight_cache_get(c, 5, 0, 1, None, None) == 1
+    assert L.fp8_weight_cache_begin_cycle(c) == 0
+    assert L.fp8_launch_count() == n0
+    L.fp8_weight_cache_destroy(c)

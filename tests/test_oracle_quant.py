@@ -136,3 +136,29 @@ def test_special_scale_cases():
     q = o.quantize_tensorwise(n, "e5m2")
     assert q["row_scale"][0] == 0.0 and np.isinf(q["row_scale_inv"][0])
     assert list(q["row"][0, :4]) == [0x7F, 0x00, 0x7F, 0x80]
+
+
+@pytest.mark.parametrize("R,C", [(144, 272), (16, 128), (128, 16), (400, 48)])
+def test_ragged_tail_blocks(R, C):
+    # a ragged tail block is quantized exactly like a standalone tensor made of
+    # the elements present (tensorwise quantization of that slice)
+    x = _inputs(R, C, 1.0, 21, outliers=0.02)
+    for fmt in ("e4m3", "e5m2"):
+        b = o.quantize_1x128(x, fmt)
+        assert b["row_scale"].shape == (R, -(-C // 128))
+        assert b["col_scale"].shape == (C, -(-R // 128))
+        c0 = (C - 1) // 128 * 128
+        i = R - 1
+        t = o.quantize_tensorwise(np.ascontiguousarray(x[i:i + 1, c0:]), fmt)
+        assert np.array_equal(b["row"][i, c0:], t["row"][0])
+        assert b["row_scale"][i, -1] == t["row_scale"][0]
+        r0 = (R - 1) // 128 * 128
+        j = C - 1
+        t = o.quantize_tensorwise(np.ascontiguousarray(x[r0:, j:j + 1]), fmt)
+        assert np.array_equal(b["col"][j, r0:], t["row"][:, 0])
+        assert b["col_scale_inv"][j, -1] == t["row_scale_inv"][0]
+        w = o.quantize_128x128(x, fmt)
+        t = o.quantize_tensorwise(np.ascontiguousarray(x[r0:, c0:]), fmt)
+        assert np.array_equal(w["row"][r0:, c0:], t["row"])
+        assert w["row_scale"][-1, -1] == t["row_scale"][0]
+        assert np.array_equal(w["col"], w["row"].T)
