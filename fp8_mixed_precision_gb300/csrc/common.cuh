@@ -55,6 +55,30 @@ __device__ __forceinline__ uint32_t cvt4(float a, float b, float c, float d) {
   return cvt2<FMT>(a, b) | (cvt2<FMT>(c, d) << 16);
 }
 
+// As cvt2 without the NaN fix-up: only for values known not to be NaN.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt2_finite(float lo, float hi) {
+  uint16_t r;
+  if (FMT == FP8_FORMAT_E4M3)
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt4_finite(float a, float b, float c, float d) {
+  return cvt2_finite<FMT>(a, b) | (cvt2_finite<FMT>(c, d) << 16);
+}
+
+// True if any bf16 of the packed pairs is inf or NaN (exponent all ones).
+__device__ __forceinline__ bool any_nonfinite_bf16(uint4 a, uint4 b) {
+  const uint32_t e = 0x7F807F80u;
+  uint32_t m = __vcmpeq2(a.x & e, e) | __vcmpeq2(a.y & e, e) | __vcmpeq2(a.z & e, e) |
+               __vcmpeq2(a.w & e, e) | __vcmpeq2(b.x & e, e) | __vcmpeq2(b.y & e, e) |
+               __vcmpeq2(b.z & e, e) | __vcmpeq2(b.w & e, e);
+  return m != 0;
+}
+
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

@@ -34,11 +34,15 @@ namespace fp8lin {
 namespace {
 
 constexpr int BM = 128, BN = 128, BK = 128;
-constexpr int kStages = 6;
+constexpr int kStages = 4;
 constexpr int kStageA = BM * BK;  // bytes
 constexpr int kStageB = BN * BK;
 constexpr int kStageBytes = kStageA + kStageB;
 constexpr int kEpiWarps = 8;
+// bf16 output staging: per epilogue warp two 32-row x 64-column buffers
+// (32 x 128 bytes, 128-byte swizzled) feeding TMA bulk-tensor stores.
+constexpr int kOutSlabBytes = 32 * 128;
+constexpr int kOutBytes = kEpiWarps * 2 * kOutSlabBytes;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 2 * BN;  // two fp32 accumulator buffers
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
@@ -67,7 +71,8 @@ struct SmemCtl {
   float bscale[kEpiWarps][64];
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + sizeof(SmemCtl);
+constexpr size_t kSmemBytes =
+    1024 + (size_t)kStages * kStageBytes + (size_t)kOutBytes + sizeof(SmemCtl);
 
 // Bounded wait on phase `parity` of `bar`; false on abort or timeout.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort) {
@@ -132,14 +137,35 @@ __device__ __forceinline__ void store32(const GemmArgs &g, int split, int64_t m,
   }
 }
 
+// Row `row` of a 32x64 bf16 output slab (128 bytes, 128-byte swizzle: the
+// 16-byte chunk j of row r sits at chunk j ^ (r & 7), which is also the
+// layout the TMA store expects); writes chunks chunk0..chunk0+3 from v*scale.
+__device__ __forceinline__ void stage32(uint8_t *slab, int row, int chunk0, const float (&v)[32],
+                                        float scale) {
+  uint8_t *rp = slab + row * 128;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(v[8 * p + 2 * j], scale),
+                                               __fmul_rn(v[8 * p + 2 * j + 1], scale));
+      w[j] = *reinterpret_cast<uint32_t *>(&b);
+    }
+    const int chunk = (chunk0 + p) ^ (row & 7);
+    *reinterpret_cast<uint4 *>(rp + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 template <int SCALING, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const GemmArgs g) {
+                    const __grid_constant__ CUtensorMap tmC, const GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  SmemCtl *ctl = reinterpret_cast<SmemCtl *>(smem + (size_t)kStages * kStageBytes);
+  uint8_t *out_stage = smem + (size_t)kStages * kStageBytes;
+  SmemCtl *ctl = reinterpret_cast<SmemCtl *>(out_stage + kOutBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -158,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmB);
+    if (!SPLIT) ptx::tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     ptx::tmem_alloc(&ctl->tmem_base, kTmemCols);
@@ -256,6 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q * 32 + lane;     // tile row owned by this thread
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 64);
     uint32_t nacc = 0;
+    uint32_t nout = 0;  // bf16 slabs this warp has handed to TMA stores
+    uint8_t *slabs = out_stage + (size_t)(warp - 2) * 2 * kOutSlabBytes;
     float s_tensor = 0.0f;
     if (SCALING == FP8_SCALING_TENSOR) s_tensor = __fmul_rn(g.a_sinv[0], g.b_sinv[0]);
     for (int64_t u = blockIdx.x; u < g.units; u += gridDim.x) {
@@ -264,25 +293,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int split = (int)(u % g.splits);
       const int64_t m = (int64_t)tm * BM + r;
       const int64_t colbase = (int64_t)tn * BN + h * 64;
+      const int64_t slab_y = (int64_t)tm * BM + q * 32;
+      // this warp's 32x64 slab holds at least one in-range element
+      const bool slab_live = slab_y < g.M && colbase < g.N;
+      uint8_t *slab = slabs + (nout & 1) * kOutSlabBytes;
+      if (!SPLIT && slab_live) {
+        // the store issued two slabs ago from this buffer has finished reading it
+        if (lane == 0) ptx::bulk_wait_read<1>();
+        __syncwarp();
+      }
       bool ok = true;
       if (SCALING == FP8_SCALING_TENSOR) {
         const uint32_t ab = nacc & 1, aph = (nacc >> 1) & 1;
         if (!wait_bar(&ctl->acc_full[ab], aph, abort)) break;
         ptx::tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t raw[32];
-          ptx::tmem_ld32(tl + ab * BN + 32 * c, raw);
-          ptx::tmem_ld_wait();
-          float v[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(raw[j]), s_tensor);
-          store32<SPLIT>(g, split, m, colbase + 32 * c, v);
-        }
+        uint32_t raw0[32], raw1[32];
+        ptx::tmem_ld32(tl + ab * BN, raw0);
+        ptx::tmem_ld32(tl + ab * BN + 32, raw1);
+        ptx::tmem_ld_wait();
+        // the accumulator is in registers: hand the TMEM buffer back to the MMA
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty[ab]);
         ++nacc;
+        float v0[32], v1[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          v0[j] = __uint_as_float(raw0[j]);
+          v1[j] = __uint_as_float(raw1[j]);
+        }
+        if (SPLIT) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            v0[j] = __fmul_rn(v0[j], s_tensor);
+            v1[j] = __fmul_rn(v1[j], s_tensor);
+          }
+          store32<true>(g, split, m, colbase, v0);
+          store32<true>(g, split, m, colbase + 32, v1);
+        } else if (slab_live) {
+          stage32(slab, lane, 0, v0, s_tensor);
+          stage32(slab, lane, 4, v1, s_tensor);
+        }
       } else {
         float acc[64];
 #pragma unroll
@@ -306,38 +357,57 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!wait_bar(&ctl->acc_full[ab], aph, abort)) { ok = false; break; }
           ptx::tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t raw[32];
-            ptx::tmem_ld32(tl + ab * BN + 32 * c, raw);
-            ptx::tmem_ld_wait();
-            if (SCALING == FP8_SCALING_1x128_128x128) {
-              const float s = __fmul_rn(sa, sb_tile);
-#pragma unroll
-              for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(__uint_as_float(raw[j]), s, acc[32 * c + j]);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const float s = __fmul_rn(sa, ctl->bscale[warp - 2][32 * c + j]);
-                acc[32 * c + j] = fmaf(__uint_as_float(raw[j]), s, acc[32 * c + j]);
-              }
-            }
-          }
+          uint32_t raw0[32], raw1[32];
+          ptx::tmem_ld32(tl + ab * BN, raw0);
+          ptx::tmem_ld32(tl + ab * BN + 32, raw1);
+          ptx::tmem_ld_wait();
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty[ab]);
           ++nacc;
+          if (SCALING == FP8_SCALING_1x128_128x128) {
+            const float s = __fmul_rn(sa, sb_tile);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              acc[j] = fmaf(__uint_as_float(raw0[j]), s, acc[j]);
+              acc[32 + j] = fmaf(__uint_as_float(raw1[j]), s, acc[32 + j]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float s0 = __fmul_rn(sa, ctl->bscale[warp - 2][j]);
+              const float s1 = __fmul_rn(sa, ctl->bscale[warp - 2][32 + j]);
+              acc[j] = fmaf(__uint_as_float(raw0[j]), s0, acc[j]);
+              acc[32 + j] = fmaf(__uint_as_float(raw1[j]), s1, acc[32 + j]);
+            }
+          }
         }
         if (!ok) break;
+        float v0[32], v1[32];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          float v[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = acc[32 * c + j];
-          store32<SPLIT>(g, split, m, colbase + 32 * c, v);
+        for (int j = 0; j < 32; ++j) {
+          v0[j] = acc[j];
+          v1[j] = acc[32 + j];
+        }
+        if (SPLIT) {
+          store32<true>(g, split, m, colbase, v0);
+          store32<true>(g, split, m, colbase + 32, v1);
+        } else if (slab_live) {
+          stage32(slab, lane, 0, v0, 1.0f);
+          stage32(slab, lane, 4, v1, 1.0f);
         }
       }
+      if (!SPLIT && slab_live) {
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_2d(&tmC, slab, (int)colbase, (int)slab_y);
+          ptx::bulk_commit();
+        }
+        ++nout;
+      }
     }
+    if (!SPLIT && lane == 0) ptx::bulk_wait<0>();  // stores complete before the CTA exits
   }
 
   ptx::tc_fence_before();
@@ -389,6 +459,20 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// bf16 [rows, cols] row-major output, boxes of 32 rows x 64 columns (128 bytes),
+// 128-byte swizzle; out-of-range parts of a box are not written.
+bool make_out_map(CUtensorMap *m, void *base, int64_t rows, int64_t cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // [rows, cols] u8 row-major, boxes of 128 rows x 128 bytes, 128-byte swizzle,
 // zero fill outside the tensor.
 bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols) {
@@ -426,8 +510,8 @@ Plan make_plan(int64_t M, int64_t N, int64_t K) {
 }
 
 template <int SCALING, bool SPLIT>
-cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g,
-                           cudaStream_t st) {
+cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
+                           const GemmArgs &g, cudaStream_t st) {
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -445,7 +529,7 @@ cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const G
   if (SCALING == FP8_SCALING_1x128_128x128) bytes += 4.0 * g.kbs * (g.M + g.tiles_n);
   if (SCALING == FP8_SCALING_1x128_1x128) bytes += 4.0 * g.kbs * (g.M + g.N);
   LaunchScope ls(names[SCALING], st, bytes, 2.0 * g.M * g.N * g.K);
-  fp8_gemm_kernel<SCALING, SPLIT><<<(unsigned)grid, kThreads, kSmemBytes, st>>>(ta, tb, g);
+  fp8_gemm_kernel<SCALING, SPLIT><<<(unsigned)grid, kThreads, kSmemBytes, st>>>(ta, tb, tc, g);
   return cudaGetLastError();
 }
 
@@ -464,8 +548,13 @@ cudaError_t launch_gemm(const uint8_t *A, int a_fmt, const float *a_sinv, const 
   if (M == 0 || N == 0) return cudaSuccess;
   if (K == 0) return cudaMemsetAsync(C, 0, (size_t)M * N * 2, st);
   const Plan p = make_plan(M, N, K);
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   if (!make_map(&ta, A, M, K) || !make_map(&tb, B, N, K)) return cudaErrorInvalidValue;
+  if (p.splits == 1) {
+    if (!make_out_map(&tc, C, M, N)) return cudaErrorInvalidValue;
+  } else {
+    tc = ta;  // unused by the split-K variant
+  }
   GemmArgs g;
   g.M = M;
   g.N = N;
@@ -486,16 +575,16 @@ cudaError_t launch_gemm(const uint8_t *A, int a_fmt, const float *a_sinv, const 
   const bool split = p.splits > 1;
   switch (scaling) {
     case FP8_SCALING_TENSOR:
-      e = split ? launch_variant<FP8_SCALING_TENSOR, true>(ta, tb, g, st)
-                : launch_variant<FP8_SCALING_TENSOR, false>(ta, tb, g, st);
+      e = split ? launch_variant<FP8_SCALING_TENSOR, true>(ta, tb, tc, g, st)
+                : launch_variant<FP8_SCALING_TENSOR, false>(ta, tb, tc, g, st);
       break;
     case FP8_SCALING_1x128_128x128:
-      e = split ? launch_variant<FP8_SCALING_1x128_128x128, true>(ta, tb, g, st)
-                : launch_variant<FP8_SCALING_1x128_128x128, false>(ta, tb, g, st);
+      e = split ? launch_variant<FP8_SCALING_1x128_128x128, true>(ta, tb, tc, g, st)
+                : launch_variant<FP8_SCALING_1x128_128x128, false>(ta, tb, tc, g, st);
       break;
     default:
-      e = split ? launch_variant<FP8_SCALING_1x128_1x128, true>(ta, tb, g, st)
-                : launch_variant<FP8_SCALING_1x128_1x128, false>(ta, tb, g, st);
+      e = split ? launch_variant<FP8_SCALING_1x128_1x128, true>(ta, tb, tc, g, st)
+                : launch_variant<FP8_SCALING_1x128_1x128, false>(ta, tb, tc, g, st);
       break;
   }
   if (e != cudaSuccess || !split) return e;

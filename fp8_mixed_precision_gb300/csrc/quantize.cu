@@ -89,11 +89,31 @@ struct QParams {
   int n_partials;
 };
 
+// A product x * scale can only be NaN when x is inf or NaN (scale is finite
+// and non-negative; inf * 0 needs an infinite x), so a row slot whose 16
+// inputs are all finite converts without the NaN fix-up.
+template <int FMT>
+__device__ __forceinline__ uint4 cast16(const float (&v)[16], bool special) {
+  uint4 q;
+  if (!special) {
+    q.x = cvt4_finite<FMT>(v[0], v[1], v[2], v[3]);
+    q.y = cvt4_finite<FMT>(v[4], v[5], v[6], v[7]);
+    q.z = cvt4_finite<FMT>(v[8], v[9], v[10], v[11]);
+    q.w = cvt4_finite<FMT>(v[12], v[13], v[14], v[15]);
+  } else {
+    q.x = cvt4<FMT>(v[0], v[1], v[2], v[3]);
+    q.y = cvt4<FMT>(v[4], v[5], v[6], v[7]);
+    q.z = cvt4<FMT>(v[8], v[9], v[10], v[11]);
+    q.w = cvt4<FMT>(v[12], v[13], v[14], v[15]);
+  }
+  return q;
+}
+
 template <int MODE, int FMT>
-__global__ void __launch_bounds__(kQThreads) quant_tile_kernel(QParams p) {
+__global__ void __launch_bounds__(kQThreads, MODE == 0 ? 4 : 2) quant_tile_kernel(QParams p) {
   __shared__ __align__(16) uint32_t tile[128 * 32];   // FP8 bytes for the transposed layout
   __shared__ float colred[8][128];                     // 1x128: per-warp column maxima
-  __shared__ float colsc[128], colsci[128];            // 1x128: column scales
+  __shared__ __align__(16) float colsc[128];           // 1x128: column scales
   __shared__ float red8[8];
   __shared__ float tscale[2];
 
@@ -224,7 +244,6 @@ __global__ void __launch_bounds__(kQThreads) quant_tile_kernel(QParams p) {
           float s, si;
           scale_from_amax(m, fmax, s, si);
           colsc[t] = s;
-          colsci[t] = si;
           if (t < cols_here) {
             p.col_scale[(c0 + t) * tiles_r + tr] = s;
             p.col_scale_inv[(c0 + t) * tiles_r + tr] = si;
@@ -235,32 +254,36 @@ __global__ void __launch_bounds__(kQThreads) quant_tile_kernel(QParams p) {
     }
 
     // ---- cast: rowwise bytes (and, for one-scale tiles, the transposed source)
+    float cs[16];
+    if (MODE == Q_BLOCK1x128 && p.out_col) {
+      const float4 *c4 = reinterpret_cast<const float4 *>(colsc + 16 * cg);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 f = c4[k];
+        cs[4 * k] = f.x; cs[4 * k + 1] = f.y; cs[4 * k + 2] = f.z; cs[4 * k + 3] = f.w;
+      }
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int r = rr + 32 * i;
+      const bool special = any_nonfinite_bf16(raw[i][0], raw[i][1]);
       const bool need_row = p.out_row || (MODE != Q_BLOCK1x128 && p.out_col);
       if (need_row) {
         const float s = rs[i];
-        uint4 q;
-        q.x = cvt4<FMT>(__fmul_rn(val(i, 0), s), __fmul_rn(val(i, 1), s), __fmul_rn(val(i, 2), s), __fmul_rn(val(i, 3), s));
-        q.y = cvt4<FMT>(__fmul_rn(val(i, 4), s), __fmul_rn(val(i, 5), s), __fmul_rn(val(i, 6), s), __fmul_rn(val(i, 7), s));
-        q.z = cvt4<FMT>(__fmul_rn(val(i, 8), s), __fmul_rn(val(i, 9), s), __fmul_rn(val(i, 10), s), __fmul_rn(val(i, 11), s));
-        q.w = cvt4<FMT>(__fmul_rn(val(i, 12), s), __fmul_rn(val(i, 13), s), __fmul_rn(val(i, 14), s), __fmul_rn(val(i, 15), s));
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(val(i, j), s);
+        const uint4 q = cast16<FMT>(v, special);
         if (p.out_row && col_ok && r < rows_here)
           *reinterpret_cast<uint4 *>(p.out_row + (r0 + r) * p.C + c0 + 16 * cg) = q;
         if (MODE != Q_BLOCK1x128 && p.out_col)
           *reinterpret_cast<uint4 *>(&tile[r * 32 + ((4 * cg) ^ swz(r))]) = q;
       }
       if (MODE == Q_BLOCK1x128 && p.out_col) {
-        float cs[16];
+        float v[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) cs[j] = __fmul_rn(val(i, j), colsc[16 * cg + j]);
-        uint4 q;
-        q.x = cvt4<FMT>(cs[0], cs[1], cs[2], cs[3]);
-        q.y = cvt4<FMT>(cs[4], cs[5], cs[6], cs[7]);
-        q.z = cvt4<FMT>(cs[8], cs[9], cs[10], cs[11]);
-        q.w = cvt4<FMT>(cs[12], cs[13], cs[14], cs[15]);
-        *reinterpret_cast<uint4 *>(&tile[r * 32 + ((4 * cg) ^ swz(r))]) = q;
+        for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(val(i, j), cs[j]);
+        *reinterpret_cast<uint4 *>(&tile[r * 32 + ((4 * cg) ^ swz(r))]) = cast16<FMT>(v, special);
       }
     }
 
