@@ -24,7 +24,7 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-r
               "-I" + INCLUDE] + ARCH
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-Wall", "-I" + INCLUDE]
 
-CU_SOURCES = ["quantize.cu", "gemm.cu", "glue.cu"]
+CU_SOURCES = ["quantize.cu", "gemm.cu", "glue.cu", "noalloc.cu"]
 CXX_SOURCES = ["api.cpp"]
 
 

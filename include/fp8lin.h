@@ -241,6 +241,35 @@ typedef struct {
 fp8_status fp8_profile_begin(void);
 fp8_status fp8_profile_end(fp8_kernel_stat *out, int cap, int *n);
 
+/* ------------------------------------------------------------------ allocation-free variant
+ * fp8_quantize_tensorwise_noalloc: the tensorwise quantizer of fp8_quantize
+ * (recipe FP8_RECIPE_TENSORWISE, same bytes and scales) for callers that
+ * cannot allocate device memory, e.g. code running inside a device allocator
+ * or memory-pool hook, latency-critical paths that must avoid cudaMalloc /
+ * cudaFree (they can synchronise the device), or plugins whose framework owns
+ * all device memory.  The reconstruction's pages have no counterpart; this
+ * is a library convenience.
+ *   The scratch between the two passes (one fp32 partial amax per CTA of the
+ *   first pass) lives in a fixed 4 KiB device array inside the library (1024
+ *   slots), held on every GPU that loads the library until exit.  The call
+ *   needs no workspace and makes no allocation; a launch that would need more
+ *   than 1024 slots returns FP8_ERR_WORKSPACE (the first pass uses at most
+ *   min(2 x SM count, 1024), so no supported size does).
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   All calls on a device share the array and it keeps the last call's
+ *   contents; each call overwrites every slot it reads, so nothing needs
+ *   clearing.  Calls whose work can overlap on the GPU (unordered streams)
+ *   race on the array and must be serialised by the caller.
+ *   x [rows, cols] bf16; rowwise_out [rows, cols] and/or colwise_out
+ *   [cols, rows] (not both NULL); scale, scale_inv: one float each.
+ * Errors: INVALID_ARG, SHAPE, ALIGN, WORKSPACE, CUDA. */
+fp8_status fp8_quantize_tensorwise_noalloc(const void *x, int64_t rows, int64_t cols,
+                                           fp8_role role, uint8_t *rowwise_out,
+                                           uint8_t *colwise_out, float *scale, float *scale_inv,
+                                           fp8_stream_t stream);
+
 /* ------------------------------------------------------------------ device status
  * Synchronises `stream`, then returns and clears the device-side status word
  * that kernels set when a bounded wait gives up (FP8_ERR_TIMEOUT) - no kernel
