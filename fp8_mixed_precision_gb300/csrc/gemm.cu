@@ -12,19 +12,22 @@
 //                             it by that block's scales and add it to an fp32
 //                             register accumulator (software promotion).
 //
-// Structure: persistent CTAs (one per SM), warp-specialised.
-//   warp 0      TMA producer: 128x128-byte A and B tiles (128B swizzle) into a
-//               kStages-deep shared-memory ring guarded by full/empty mbarriers
-//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
-//               (kind::f8f6f4, M=128, N=128, K=32 per instruction)
-//   warps 2-9   epilogue: tcgen05.ld from TMEM, scale, round to bf16, store.
+// Structure: persistent CTAs (one per SM), warp-specialised, tile BM x BN
+// (128 x 256 for tensor scaling when N allows, else 128 x 128).
+//   warp 0      TMA producer: A (128 rows) and B (BN rows) tiles of 128 bytes
+//               along K, 128B swizzle, into a shared-memory ring guarded by
+//               full/empty mbarriers
+//   warp 1      TMEM allocator (all 512 columns) + single-thread tcgen05.mma
+//               issuer (kind::f8f6f4, M = 128, N = BN, K = 32 per instruction)
+//   warps 2-9   epilogue: tcgen05.ld from TMEM, scale, round to bf16, stage
+//               32x64 slabs in 128B-swizzled shared memory, TMA bulk stores.
 //               Warp w reads TMEM lanes 32*(w%4)..+31 and column half (w-2)/4.
-// The MMA writes two TMEM buffers alternately so the epilogue of one tile
-// (tensor scaling) or of one K block (block scaling) overlaps the next MMAs.
-// Split-K (small M*N, deep K): each split writes an fp32 partial to the
-// workspace; a second kernel sums the splits in a fixed order.  Every wait is
-// bounded: on expiry the kernel records FP8_ERR_TIMEOUT, drains what it has in
-// flight, frees its TMEM and returns.
+// TMEM holds 512/BN accumulator buffers used round-robin, so the epilogue of
+// one tile (tensor scaling) or one K block (block scaling) overlaps the
+// following MMAs.  Split-K (small M*N, deep K): each split writes an fp32
+// partial to the workspace; a second kernel sums the splits in a fixed
+// order.  Every wait is bounded: on expiry the kernel records
+// FP8_ERR_TIMEOUT, drains what it has in flight, frees its TMEM and returns.
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -33,21 +36,35 @@ namespace fp8lin {
 
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 128;
-constexpr int kStages = 4;
-constexpr int kStageA = BM * BK;  // bytes
-constexpr int kStageB = BN * BK;
-constexpr int kStageBytes = kStageA + kStageB;
+constexpr int BM = 128, BK = 128;
 constexpr int kEpiWarps = 8;
-// bf16 output staging: per epilogue warp two 32-row x 64-column buffers
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr uint32_t kTmemCols = 512;
+// bf16 output staging: per epilogue warp two 32-row x 64-column slabs
 // (32 x 128 bytes, 128-byte swizzled) feeding TMA bulk-tensor stores.
 constexpr int kOutSlabBytes = 32 * 128;
 constexpr int kOutBytes = kEpiWarps * 2 * kOutSlabBytes;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr uint32_t kTmemCols = 2 * BN;  // two fp32 accumulator buffers
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
-constexpr uint64_t kDrainLimitNs = 100000000ull;   // 0.1 s
-constexpr int kSplitTargetCtas = 152;              // split-K fills about this many CTAs
+constexpr int kSmemBudget = 227 * 1024;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s
+constexpr int kSplitTargetCtas = 152;             // split-K fills about this many CTAs
+constexpr int kMaxStages = 8;
+
+template <int BN>
+struct Cfg {
+  static constexpr int kStageA = BM * BK;  // bytes
+  static constexpr int kStageB = BN * BK;
+  static constexpr int kStageBytes = kStageA + kStageB;
+  static constexpr int kAccBufs = (int)kTmemCols / BN;
+  static constexpr int kCtlBytes = 4096;
+  static constexpr int kStages =
+      (kSmemBudget - 1024 - kOutBytes - kCtlBytes) / kStageBytes < kMaxStages
+          ? (kSmemBudget - 1024 - kOutBytes - kCtlBytes) / kStageBytes
+          : kMaxStages;
+  static constexpr size_t kSmemBytes =
+      1024 + (size_t)kStages * kStageBytes + (size_t)kOutBytes + kCtlBytes;
+  static_assert(kStages >= 2, "shared memory too small for the operand ring");
+};
 
 __device__ unsigned g_gemm_status;
 
@@ -63,16 +80,14 @@ struct GemmArgs {
 };
 
 struct SmemCtl {
-  uint64_t full[kStages], empty[kStages];
-  uint64_t acc_full[2], acc_empty[2];
+  uint64_t full[kMaxStages], empty[kMaxStages];
+  uint64_t acc_full[4], acc_empty[4];
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
   float bscale[kEpiWarps][64];
 };
-
-constexpr size_t kSmemBytes =
-    1024 + (size_t)kStages * kStageBytes + (size_t)kOutBytes + sizeof(SmemCtl);
+static_assert(sizeof(SmemCtl) <= 4096, "control block");
 
 // Bounded wait on phase `parity` of `bar`; false on abort or timeout.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort) {
@@ -111,29 +126,21 @@ __device__ __forceinline__ void decode_unit(const GemmArgs &g, int64_t u, int &t
   kb1 = min(g.kbs, kb0 + g.kb_per_split);
 }
 
-// Write 32 consecutive outputs of row m starting at column col0.
-template <bool SPLIT>
-__device__ __forceinline__ void store32(const GemmArgs &g, int split, int64_t m, int64_t col0,
-                                        const float (&v)[32]) {
+// fp32 split-K partial: 32 consecutive outputs of row m from column col0.
+__device__ __forceinline__ void store32_f32(const GemmArgs &g, int split, int64_t m, int64_t col0,
+                                            const float (&v)[32], float scale) {
   if (m >= g.M) return;
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
     const int64_t n = col0 + 8 * p;
     if (n >= g.N) continue;
-    if (SPLIT) {
-      float *dst = static_cast<float *>(g.out) + ((int64_t)split * g.M + m) * g.N + n;
-      reinterpret_cast<float4 *>(dst)[0] = make_float4(v[8 * p], v[8 * p + 1], v[8 * p + 2], v[8 * p + 3]);
-      reinterpret_cast<float4 *>(dst)[1] = make_float4(v[8 * p + 4], v[8 * p + 5], v[8 * p + 6], v[8 * p + 7]);
-    } else {
-      uint32_t w[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * p + 2 * j], v[8 * p + 2 * j + 1]);
-        w[j] = *reinterpret_cast<uint32_t *>(&b);
-      }
-      __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(g.out) + m * g.N + n;
-      *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
+    float *dst = static_cast<float *>(g.out) + ((int64_t)split * g.M + m) * g.N + n;
+    reinterpret_cast<float4 *>(dst)[0] =
+        make_float4(__fmul_rn(v[8 * p], scale), __fmul_rn(v[8 * p + 1], scale),
+                    __fmul_rn(v[8 * p + 2], scale), __fmul_rn(v[8 * p + 3], scale));
+    reinterpret_cast<float4 *>(dst)[1] =
+        make_float4(__fmul_rn(v[8 * p + 4], scale), __fmul_rn(v[8 * p + 5], scale),
+                    __fmul_rn(v[8 * p + 6], scale), __fmul_rn(v[8 * p + 7], scale));
   }
 }
 
@@ -157,14 +164,41 @@ __device__ __forceinline__ void stage32(uint8_t *slab, int row, int chunk0, cons
   }
 }
 
-template <int SCALING, bool SPLIT>
+// Packed fp32 pair arithmetic (two IEEE operations per instruction).
+__device__ __forceinline__ uint64_t pk(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk(uint64_t r, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+template <int SCALING, bool SPLIT, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const GemmArgs g) {
+  using C = Cfg<BN>;
+  constexpr int kStages = C::kStages;
+  constexpr int NB = C::kAccBufs;
+  constexpr int kHalf = BN / 2;           // columns per epilogue warp
+  constexpr int kSlabs = kHalf / 64;      // 64-column slabs per epilogue warp per tile
+  static_assert(SCALING == FP8_SCALING_TENSOR || BN == 128, "block scaling uses 128-wide tiles");
+
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t *out_stage = smem + (size_t)kStages * kStageBytes;
+  uint8_t *out_stage = smem + (size_t)kStages * C::kStageBytes;
   SmemCtl *ctl = reinterpret_cast<SmemCtl *>(out_stage + kOutBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -173,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&ctl->full[s], 1);
       ptx::mbar_init(&ctl->empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NB; ++b) {
       ptx::mbar_init(&ctl->acc_full[b], 1);
       ptx::mbar_init(&ctl->acc_empty[b], kEpiWarps);
     }
@@ -209,10 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         decode_unit(g, u, tm, tn, kb0, kb1);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bar(&ctl->empty[stage], phase ^ 1, abort)) { ok = false; break; }
-          uint8_t *sa = smem + (size_t)stage * kStageBytes;
-          ptx::mbar_arrive_expect_tx(&ctl->full[stage], kStageBytes);
+          uint8_t *sa = smem + (size_t)stage * C::kStageBytes;
+          ptx::mbar_arrive_expect_tx(&ctl->full[stage], C::kStageBytes);
           ptx::tma_load_2d(sa, &tmA, &ctl->full[stage], kb * BK, tm * BM);
-          ptx::tma_load_2d(sa + kStageA, &tmB, &ctl->full[stage], kb * BK, tn * BN);
+          ptx::tma_load_2d(sa + C::kStageA, &tmB, &ctl->full[stage], kb * BK, tn * BN);
           last_phase[stage] = (int)phase;
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
@@ -231,45 +265,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
         int tm, tn, kb0, kb1;
         decode_unit(g, u, tm, tn, kb0, kb1);
-        if (SCALING == FP8_SCALING_TENSOR) {
-          const uint32_t ab = nacc & 1, aph = (nacc >> 1) & 1;
-          if (!wait_bar(&ctl->acc_empty[ab], aph ^ 1, abort)) { ok = false; break; }
-          ptx::tc_fence_after();
-          const uint32_t d = tmem + ab * BN;
-          for (int kb = kb0; kb < kb1; ++kb) {
-            if (!wait_bar(&ctl->full[stage], phase, abort)) { ok = false; break; }
-            ptx::tc_fence_after();
-            const uint32_t a_addr = ptx::smem_u32(smem + (size_t)stage * kStageBytes);
-            const uint64_t adesc = ptx::smem_desc_sw128(a_addr);
-            const uint64_t bdesc = ptx::smem_desc_sw128(a_addr + kStageA);
-#pragma unroll
-            for (int k = 0; k < BK / 32; ++k)
-              ptx::mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, g.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-            ptx::mma_commit(&ctl->empty[stage]);
-            if (++stage == kStages) { stage = 0; phase ^= 1; }
-          }
-          if (!ok) break;
-          ptx::mma_commit(&ctl->acc_full[ab]);
-          ++nacc;
-        } else {
-          for (int kb = kb0; kb < kb1; ++kb) {
-            const uint32_t ab = nacc & 1, aph = (nacc >> 1) & 1;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          // tensor scaling: one accumulator per tile; block scaling: one per K block
+          const bool first = SCALING != FP8_SCALING_TENSOR || kb == kb0;
+          const bool last = SCALING != FP8_SCALING_TENSOR || kb == kb1 - 1;
+          const uint32_t ab = nacc % NB, aph = (nacc / NB) & 1;
+          if (first) {
             if (!wait_bar(&ctl->acc_empty[ab], aph ^ 1, abort)) { ok = false; break; }
             ptx::tc_fence_after();
-            if (!wait_bar(&ctl->full[stage], phase, abort)) { ok = false; break; }
-            ptx::tc_fence_after();
-            const uint32_t d = tmem + ab * BN;
-            const uint32_t a_addr = ptx::smem_u32(smem + (size_t)stage * kStageBytes);
-            const uint64_t adesc = ptx::smem_desc_sw128(a_addr);
-            const uint64_t bdesc = ptx::smem_desc_sw128(a_addr + kStageA);
+          }
+          if (!wait_bar(&ctl->full[stage], phase, abort)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t d = tmem + ab * BN;
+          const uint32_t a_addr = ptx::smem_u32(smem + (size_t)stage * C::kStageBytes);
+          const uint64_t adesc = ptx::smem_desc_sw128(a_addr);
+          const uint64_t bdesc = ptx::smem_desc_sw128(a_addr + C::kStageA);
 #pragma unroll
-            for (int k = 0; k < BK / 32; ++k)
-              ptx::mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, g.idesc, k > 0 ? 1u : 0u);
-            ptx::mma_commit(&ctl->empty[stage]);
+          for (int k = 0; k < BK / 32; ++k)
+            ptx::mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, g.idesc, (!first || k > 0) ? 1u : 0u);
+          ptx::mma_commit(&ctl->empty[stage]);
+          if (last) {
             ptx::mma_commit(&ctl->acc_full[ab]);
             ++nacc;
-            if (++stage == kStages) { stage = 0; phase ^= 1; }
           }
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
       // all issued MMAs complete before TMEM is freed / the CTA exits
@@ -281,79 +300,101 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;          // TMEM lane quarter this warp may access
     const int h = (warp - 2) >> 2;   // column half of the tile
     const int r = q * 32 + lane;     // tile row owned by this thread
-    const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 64);
+    const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * kHalf);
     uint32_t nacc = 0;
     uint32_t nout = 0;  // bf16 slabs this warp has handed to TMA stores
     uint8_t *slabs = out_stage + (size_t)(warp - 2) * 2 * kOutSlabBytes;
     float s_tensor = 0.0f;
     if (SCALING == FP8_SCALING_TENSOR) s_tensor = __fmul_rn(g.a_sinv[0], g.b_sinv[0]);
+
+    // Hands one 32x64 slab (columns col0.. of rows slab_y..) to a TMA store
+    // (bf16) or writes it as an fp32 split-K partial.
+    auto emit = [&](const float (&v0)[32], const float (&v1)[32], float scale, int64_t col0,
+                    int64_t slab_y, int split) {
+      if (SPLIT) {
+        store32_f32(g, split, slab_y + lane, col0, v0, scale);
+        store32_f32(g, split, slab_y + lane, col0 + 32, v1, scale);
+        return;
+      }
+      if (slab_y >= g.M || col0 >= g.N) return;  // slab entirely outside C
+      uint8_t *slab = slabs + (nout & 1) * kOutSlabBytes;
+      if (lane == 0) ptx::bulk_wait_read<1>();  // the store two slabs ago has read this buffer
+      __syncwarp();
+      stage32(slab, lane, 0, v0, scale);
+      stage32(slab, lane, 4, v1, scale);
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tma_store_2d(&tmC, slab, (int)col0, (int)slab_y);
+        ptx::bulk_commit();
+      }
+      ++nout;
+    };
+
     for (int64_t u = blockIdx.x; u < g.units; u += gridDim.x) {
       int tm, tn, kb0, kb1;
       decode_unit(g, u, tm, tn, kb0, kb1);
       const int split = (int)(u % g.splits);
       const int64_t m = (int64_t)tm * BM + r;
-      const int64_t colbase = (int64_t)tn * BN + h * 64;
+      const int64_t colbase = (int64_t)tn * BN + h * kHalf;
       const int64_t slab_y = (int64_t)tm * BM + q * 32;
-      // this warp's 32x64 slab holds at least one in-range element
-      const bool slab_live = slab_y < g.M && colbase < g.N;
-      uint8_t *slab = slabs + (nout & 1) * kOutSlabBytes;
-      if (!SPLIT && slab_live) {
-        // the store issued two slabs ago from this buffer has finished reading it
-        if (lane == 0) ptx::bulk_wait_read<1>();
-        __syncwarp();
-      }
-      bool ok = true;
       if (SCALING == FP8_SCALING_TENSOR) {
-        const uint32_t ab = nacc & 1, aph = (nacc >> 1) & 1;
+        const uint32_t ab = nacc % NB, aph = (nacc / NB) & 1;
         if (!wait_bar(&ctl->acc_full[ab], aph, abort)) break;
         ptx::tc_fence_after();
-        uint32_t raw0[32], raw1[32];
-        ptx::tmem_ld32(tl + ab * BN, raw0);
-        ptx::tmem_ld32(tl + ab * BN + 32, raw1);
-        ptx::tmem_ld_wait();
-        // the accumulator is in registers: hand the TMEM buffer back to the MMA
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty[ab]);
-        ++nacc;
-        float v0[32], v1[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          v0[j] = __uint_as_float(raw0[j]);
-          v1[j] = __uint_as_float(raw1[j]);
-        }
-        if (SPLIT) {
+        for (int s = 0; s < kSlabs; ++s) {
+          uint32_t raw0[32], raw1[32];
+          ptx::tmem_ld32(tl + ab * BN + 64 * s, raw0);
+          ptx::tmem_ld32(tl + ab * BN + 64 * s + 32, raw1);
+          ptx::tmem_ld_wait();
+          if (s == kSlabs - 1) {  // accumulator fully in registers: free the TMEM buffer
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty[ab]);
+          }
+          float v0[32], v1[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            v0[j] = __fmul_rn(v0[j], s_tensor);
-            v1[j] = __fmul_rn(v1[j], s_tensor);
+            v0[j] = __uint_as_float(raw0[j]);
+            v1[j] = __uint_as_float(raw1[j]);
           }
-          store32<true>(g, split, m, colbase, v0);
-          store32<true>(g, split, m, colbase + 32, v1);
-        } else if (slab_live) {
-          stage32(slab, lane, 0, v0, s_tensor);
-          stage32(slab, lane, 4, v1, s_tensor);
+          emit(v0, v1, s_tensor, colbase + 64 * s, slab_y, split);
         }
+        ++nacc;
       } else {
-        float acc[64];
+        uint64_t acc[32];  // 64 fp32 accumulators as packed pairs
 #pragma unroll
-        for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+        for (int j = 0; j < 32; ++j) acc[j] = 0;
         const int64_t mrow = m < g.M ? m : g.M - 1;  // clamp for the scale read only
+        const float *arow = g.a_sinv + mrow * g.lds_a;
+        // scales of the current K block, loaded one block ahead
+        float sa = arow[kb0], sb_t = 0.0f, sbl0 = 0.0f, sbl1 = 0.0f;
+        const int64_t n0 = colbase + lane, n1 = colbase + 32 + lane;
+        if (SCALING == FP8_SCALING_1x128_128x128) {
+          sb_t = g.b_sinv[(int64_t)tn * g.lds_b + kb0];
+        } else {
+          sbl0 = n0 < g.N ? g.b_sinv[n0 * g.lds_b + kb0] : 0.0f;
+          sbl1 = n1 < g.N ? g.b_sinv[n1 * g.lds_b + kb0] : 0.0f;
+        }
+        bool ok = true;
         for (int kb = kb0; kb < kb1; ++kb) {
-          const uint32_t ab = nacc & 1, aph = (nacc >> 1) & 1;
-          const float sa = g.a_sinv[mrow * g.lds_a + kb];
-          float sb_tile = 0.0f;
-          if (SCALING == FP8_SCALING_1x128_128x128) {
-            sb_tile = g.b_sinv[(int64_t)tn * g.lds_b + kb];
-          } else {
+          const uint32_t ab = nacc % NB, aph = (nacc / NB) & 1;
+          const float sa_cur = sa, sbt_cur = sb_t;
+          if (SCALING == FP8_SCALING_1x128_1x128) {
             __syncwarp();
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              const int64_t n = colbase + 32 * c + lane;
-              ctl->bscale[warp - 2][32 * c + lane] =
-                  n < g.N ? g.b_sinv[n * g.lds_b + kb] : 0.0f;
+            ctl->bscale[warp - 2][lane] = sbl0;
+            ctl->bscale[warp - 2][32 + lane] = sbl1;
+            __syncwarp();
+          }
+          if (kb + 1 < kb1) {  // prefetch the next block's scales
+            sa = arow[kb + 1];
+            if (SCALING == FP8_SCALING_1x128_128x128) {
+              sb_t = g.b_sinv[(int64_t)tn * g.lds_b + kb + 1];
+            } else {
+              sbl0 = n0 < g.N ? g.b_sinv[n0 * g.lds_b + kb + 1] : 0.0f;
+              sbl1 = n1 < g.N ? g.b_sinv[n1 * g.lds_b + kb + 1] : 0.0f;
             }
-            __syncwarp();
           }
           if (!wait_bar(&ctl->acc_full[ab], aph, abort)) { ok = false; break; }
           ptx::tc_fence_after();
@@ -366,45 +407,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty[ab]);
           ++nacc;
           if (SCALING == FP8_SCALING_1x128_128x128) {
-            const float s = __fmul_rn(sa, sb_tile);
+            const float s = __fmul_rn(sa_cur, sbt_cur);
+            const uint64_t s2 = pk(s, s);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              acc[j] = fmaf(__uint_as_float(raw0[j]), s, acc[j]);
-              acc[32 + j] = fmaf(__uint_as_float(raw1[j]), s, acc[32 + j]);
+            for (int j = 0; j < 16; ++j) {
+              acc[j] = fma2(pk(__uint_as_float(raw0[2 * j]), __uint_as_float(raw0[2 * j + 1])), s2,
+                            acc[j]);
+              acc[16 + j] = fma2(pk(__uint_as_float(raw1[2 * j]), __uint_as_float(raw1[2 * j + 1])),
+                                 s2, acc[16 + j]);
             }
           } else {
+            const uint64_t sa2 = pk(sa_cur, sa_cur);
+            const uint64_t *bs = reinterpret_cast<const uint64_t *>(ctl->bscale[warp - 2]);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float s0 = __fmul_rn(sa, ctl->bscale[warp - 2][j]);
-              const float s1 = __fmul_rn(sa, ctl->bscale[warp - 2][32 + j]);
-              acc[j] = fmaf(__uint_as_float(raw0[j]), s0, acc[j]);
-              acc[32 + j] = fmaf(__uint_as_float(raw1[j]), s1, acc[32 + j]);
+            for (int j = 0; j < 16; ++j) {
+              const uint64_t s0 = mul2(sa2, bs[j]), s1 = mul2(sa2, bs[16 + j]);
+              acc[j] = fma2(pk(__uint_as_float(raw0[2 * j]), __uint_as_float(raw0[2 * j + 1])), s0,
+                            acc[j]);
+              acc[16 + j] = fma2(pk(__uint_as_float(raw1[2 * j]), __uint_as_float(raw1[2 * j + 1])),
+                                 s1, acc[16 + j]);
             }
           }
         }
         if (!ok) break;
         float v0[32], v1[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          v0[j] = acc[j];
-          v1[j] = acc[32 + j];
+        for (int j = 0; j < 16; ++j) {
+          upk(acc[j], v0[2 * j], v0[2 * j + 1]);
+          upk(acc[16 + j], v1[2 * j], v1[2 * j + 1]);
         }
-        if (SPLIT) {
-          store32<true>(g, split, m, colbase, v0);
-          store32<true>(g, split, m, colbase + 32, v1);
-        } else if (slab_live) {
-          stage32(slab, lane, 0, v0, 1.0f);
-          stage32(slab, lane, 4, v1, 1.0f);
-        }
-      }
-      if (!SPLIT && slab_live) {
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          ptx::tma_store_2d(&tmC, slab, (int)colbase, (int)slab_y);
-          ptx::bulk_commit();
-        }
-        ++nout;
+        emit(v0, v1, 1.0f, colbase, slab_y, split);
       }
     }
     if (!SPLIT && lane == 0) ptx::bulk_wait<0>();  // stores complete before the CTA exits
@@ -473,14 +505,14 @@ bool make_out_map(CUtensorMap *m, void *base, int64_t rows, int64_t cols) {
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [rows, cols] u8 row-major, boxes of 128 rows x 128 bytes, 128-byte swizzle,
-// zero fill outside the tensor.
-bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols) {
+// [rows, cols] u8 row-major operand, boxes of box_rows rows x 128 bytes,
+// 128-byte swizzle, zero fill outside the tensor.
+bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)cols};
-  cuuint32_t box[2] = {128, 128};
+  cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -488,13 +520,15 @@ bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols) {
 }
 
 struct Plan {
-  int tiles_m, tiles_n, kbs, splits, kb_per_split;
+  int bn, tiles_m, tiles_n, kbs, splits, kb_per_split;
 };
 
-Plan make_plan(int64_t M, int64_t N, int64_t K) {
+// Kernel configuration as a function of (M, N, K, scaling) only.
+Plan make_plan(int64_t M, int64_t N, int64_t K, int scaling) {
   Plan p;
+  p.bn = (scaling == FP8_SCALING_TENSOR && N >= 256) ? 256 : 128;
   p.tiles_m = (int)((M + BM - 1) / BM);
-  p.tiles_n = (int)((N + BN - 1) / BN);
+  p.tiles_n = (int)((N + p.bn - 1) / p.bn);
   p.kbs = (int)((K + BK - 1) / BK);
   const int64_t tiles = (int64_t)p.tiles_m * p.tiles_n;
   int s = 1;
@@ -509,15 +543,17 @@ Plan make_plan(int64_t M, int64_t N, int64_t K) {
   return p;
 }
 
-template <int SCALING, bool SPLIT>
+template <int SCALING, bool SPLIT, int BN>
 cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
                            const GemmArgs &g, cudaStream_t st) {
+  using C = Cfg<BN>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(fp8_gemm_kernel<SCALING, SPLIT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(fp8_gemm_kernel<SCALING, SPLIT, BN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
@@ -529,29 +565,41 @@ cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const C
   if (SCALING == FP8_SCALING_1x128_128x128) bytes += 4.0 * g.kbs * (g.M + g.tiles_n);
   if (SCALING == FP8_SCALING_1x128_1x128) bytes += 4.0 * g.kbs * (g.M + g.N);
   LaunchScope ls(names[SCALING], st, bytes, 2.0 * g.M * g.N * g.K);
-  fp8_gemm_kernel<SCALING, SPLIT><<<(unsigned)grid, kThreads, kSmemBytes, st>>>(ta, tb, tc, g);
+  fp8_gemm_kernel<SCALING, SPLIT, BN><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(ta, tb, tc,
+                                                                                       g);
   return cudaGetLastError();
+}
+
+template <int SCALING>
+cudaError_t launch_scaling(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
+                           const GemmArgs &g, bool split, int bn, cudaStream_t st) {
+  if constexpr (SCALING == FP8_SCALING_TENSOR) {
+    if (bn == 256)
+      return split ? launch_variant<SCALING, true, 256>(ta, tb, tc, g, st)
+                   : launch_variant<SCALING, false, 256>(ta, tb, tc, g, st);
+  }
+  return split ? launch_variant<SCALING, true, 128>(ta, tb, tc, g, st)
+               : launch_variant<SCALING, false, 128>(ta, tb, tc, g, st);
 }
 
 }  // namespace
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int scaling) {
-  (void)scaling;
   if (M <= 0 || N <= 0 || K <= 0) return 0;
-  const Plan p = make_plan(M, N, K);
+  const Plan p = make_plan(M, N, K, scaling);
   return p.splits > 1 ? (size_t)p.splits * (size_t)M * (size_t)N * sizeof(float) : 0;
 }
 
 cudaError_t launch_gemm(const uint8_t *A, int a_fmt, const float *a_sinv, const uint8_t *B,
                         int b_fmt, const float *b_sinv, int64_t M, int64_t N, int64_t K,
-                        int scaling, void *C, void *ws, cudaStream_t st) {
+                        int scaling, void *Cout, void *ws, cudaStream_t st) {
   if (M == 0 || N == 0) return cudaSuccess;
-  if (K == 0) return cudaMemsetAsync(C, 0, (size_t)M * N * 2, st);
-  const Plan p = make_plan(M, N, K);
+  if (K == 0) return cudaMemsetAsync(Cout, 0, (size_t)M * N * 2, st);
+  const Plan p = make_plan(M, N, K, scaling);
   CUtensorMap ta, tb, tc;
-  if (!make_map(&ta, A, M, K) || !make_map(&tb, B, N, K)) return cudaErrorInvalidValue;
+  if (!make_map(&ta, A, M, K, BM) || !make_map(&tb, B, N, K, p.bn)) return cudaErrorInvalidValue;
   if (p.splits == 1) {
-    if (!make_out_map(&tc, C, M, N)) return cudaErrorInvalidValue;
+    if (!make_out_map(&tc, Cout, M, N)) return cudaErrorInvalidValue;
   } else {
     tc = ta;  // unused by the split-K variant
   }
@@ -569,22 +617,19 @@ cudaError_t launch_gemm(const uint8_t *A, int a_fmt, const float *a_sinv, const 
   g.b_sinv = b_sinv;
   g.lds_a = p.kbs;
   g.lds_b = p.kbs;
-  g.out = p.splits > 1 ? ws : C;
-  g.idesc = ptx::idesc_f8f6f4((uint32_t)a_fmt, (uint32_t)b_fmt, BM, BN);
-  cudaError_t e;
+  g.out = p.splits > 1 ? ws : Cout;
+  g.idesc = ptx::idesc_f8f6f4((uint32_t)a_fmt, (uint32_t)b_fmt, BM, (uint32_t)p.bn);
   const bool split = p.splits > 1;
+  cudaError_t e;
   switch (scaling) {
     case FP8_SCALING_TENSOR:
-      e = split ? launch_variant<FP8_SCALING_TENSOR, true>(ta, tb, tc, g, st)
-                : launch_variant<FP8_SCALING_TENSOR, false>(ta, tb, tc, g, st);
+      e = launch_scaling<FP8_SCALING_TENSOR>(ta, tb, tc, g, split, p.bn, st);
       break;
     case FP8_SCALING_1x128_128x128:
-      e = split ? launch_variant<FP8_SCALING_1x128_128x128, true>(ta, tb, tc, g, st)
-                : launch_variant<FP8_SCALING_1x128_128x128, false>(ta, tb, tc, g, st);
+      e = launch_scaling<FP8_SCALING_1x128_128x128>(ta, tb, tc, g, split, p.bn, st);
       break;
     default:
-      e = split ? launch_variant<FP8_SCALING_1x128_1x128, true>(ta, tb, tc, g, st)
-                : launch_variant<FP8_SCALING_1x128_1x128, false>(ta, tb, tc, g, st);
+      e = launch_scaling<FP8_SCALING_1x128_1x128>(ta, tb, tc, g, split, p.bn, st);
       break;
   }
   if (e != cudaSuccess || !split) return e;
@@ -592,7 +637,7 @@ cudaError_t launch_gemm(const uint8_t *A, int a_fmt, const float *a_sinv, const 
   const int64_t blocks = std::min<int64_t>((mn / 4 + 255) / 256, (int64_t)num_sms() * 8);
   LaunchScope ls("gemm_splitk_reduce", st, 4.0 * p.splits * mn + 2.0 * mn, (double)p.splits * mn);
   splitk_reduce_kernel<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, st>>>(
-      static_cast<const float *>(ws), p.splits, mn, static_cast<__nv_bfloat16 *>(C));
+      static_cast<const float *>(ws), p.splits, mn, static_cast<__nv_bfloat16 *>(Cout));
   return cudaGetLastError();
 }
 
