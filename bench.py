@@ -276,6 +276,15 @@ def run_ours(args):
     # ---- end to end through the C ABI with host buffers
     e2e = run_e2e(fp, layers, cache, ws, ctx, N, dev, world, args, stream)
 
+    # ---- the MLP-level workloads (weight caching, block MLPs)
+    workloads = None
+    if not args.no_mlp:
+        del layers
+        workloads = run_mlp_workloads(fp, dev, stream)
+        peaks_fp8 = fp8_peak
+        lb = workloads["large_block_mlp_4096_14336"]
+        lb["gemm_frac_of_fp8_peak"] = lb["gemm_tflops"] / peaks_fp8
+
     # ---- CPU baseline (rank 0, one GPU only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -306,6 +315,7 @@ def run_ours(args):
             "gpu_launches": n_launch,
             "clocks": clocks,
             "kernels": kernels,
+            "workloads": workloads,
             "baseline_note": "vs_baseline divides by the RTX 4090 fused-layout FP8 figures of "
                              "the reconstruction's table (context only)",
         }
@@ -337,9 +347,102 @@ def _traffic_for(name):
         return None
 
 
+def run_mlp_workloads(fp, dev, stream):
+    """The MLP-level workloads, timed with CUDA events on the launching stream:
+    weight caching in an 8-layer block-scaled stack under GA = 4 (cached vs
+    uncached step time, bitwise comparison of outputs and accumulated
+    gradients at full size), the d=512/ffn=2048 block MLP, and the large
+    block-scaled MLP (d=4096, ffn=14336, 16384 tokens, 1% x100 outliers)."""
+    import torch
+    from fp8_mixed_precision_gb300 import synthetic as syn
+    from fp8_mixed_precision_gb300.mlp import FP8MLPStack
+    out = {}
+
+    def timed(fn, reps):
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for _ in range(reps):
+            fn()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / reps
+
+    # ---- weight caching: 8 layers (16 FP8 linears), d=512, ffn=2048, GA=4 x 131072 tokens
+    d, ffn, L, N, GA = 512, 2048, 8, 131072, 4
+    xs = [syn.bf16_normal((N, d), 1.0, 700 + i, device=dev) for i in range(GA)]
+    dys = [syn.bf16_normal((N, d), 1e-3, 800 + i, device=dev) for i in range(GA)]
+    stk = FP8MLPStack(d, ffn, L, N, "block", device=dev)
+    res, grads = {}, {}
+    for use in (False, True):
+        stk.step(xs, dys, use, keep_outputs=False)
+    times = {False: [], True: []}
+    for _ in range(3):                      # interleaved rounds against drift
+        for use in (False, True):
+            times[use].append(timed(lambda: stk.step(xs, dys, use, keep_outputs=False), 2))
+    for use in (False, True):               # full-size bitwise comparison
+        outs = stk.step(xs, dys, use, keep_outputs=True)
+        res[use] = outs
+        grads[use] = [t.clone() for t in stk.dw1 + stk.dw2]
+    torch.cuda.synchronize()
+    same = all(torch.equal(a.view(torch.int16), b.view(torch.int16))
+               for (ya, da), (yb, db) in zip(res[False], res[True]) for a, b in ((ya, yb), (da, db)))
+    same = same and all(torch.equal(a.view(torch.int32), b.view(torch.int32))
+                        for a, b in zip(grads[False], grads[True]))
+    med = {k: statistics.median(v) for k, v in times.items()}
+    out["weight_cache_stack"] = {
+        "workload": "8-layer MLP stack (16 FP8 linears, d=512, ffn=2048), GA=4 x 131072 tokens, "
+                    "block scaling",
+        "ms_per_step_uncached": med[False], "ms_per_step_cached": med[True],
+        "reduction_pct": 100.0 * (med[False] - med[True]) / med[False],
+        "samples_uncached": times[False], "samples_cached": times[True],
+        "bitwise_identical": bool(same),
+        "weight_quantizations_per_step": {"uncached": 2 * L * GA, "cached": 2 * L},
+        "tokens_per_s_cached": GA * N / (med[True] / 1e3)}
+    del stk, xs, dys, res, grads
+    torch.cuda.empty_cache()
+
+    # ---- block MLP d=512, ffn=2048, 131072 tokens (one microbatch, fwd + bwd)
+    blk = FP8MLPStack(512, 2048, 1, 131072, "block", device=dev)
+    x = syn.bf16_normal((131072, 512), 1.0, syn.SEED_X, device=dev)
+    dy = syn.bf16_normal((131072, 512), 1e-3, syn.SEED_DY, device=dev)
+    blk.step([x], [dy], True, keep_outputs=False)
+    ms = timed(lambda: blk.step([x], [dy], True, keep_outputs=False), 5)
+    out["block_mlp_512_2048"] = {"ms_per_step": ms, "tokens_per_s": 131072 / (ms / 1e3),
+                                 "tflops": 6 * 2 * 131072 * 512 * 2048 / (ms / 1e3) / 1e12}
+    del blk, x, dy
+    torch.cuda.empty_cache()
+
+    # ---- large block MLP d=4096, ffn=14336, 16384 tokens, 1% x100 outliers
+    big = FP8MLPStack(4096, 14336, 1, 16384, "block", device=dev)
+    x = syn.bf16_normal((16384, 4096), 1.0, syn.SEED_X, device=dev, outlier_frac=0.01)
+    dy = syn.bf16_normal((16384, 4096), 1e-3, syn.SEED_DY, device=dev)
+    big.step([x], [dy], True, keep_outputs=False)
+    torch.cuda.synchronize()
+    fp.fp8_profile_begin()
+    ms = timed(lambda: big.step([x], [dy], True, keep_outputs=False), 3)
+    ks = fp.fp8_profile_end()
+    gemm = [k for k in ks if k["name"].startswith("gemm_fp8")]
+    g_ms = sum(k["total_ms"] for k in gemm)
+    g_fl = sum(k["flops"] for k in gemm)
+    out["large_block_mlp_4096_14336"] = {
+        "ms_per_step": ms, "tokens_per_s": 16384 / (ms / 1e3),
+        "gemm_tflops": g_fl / (g_ms / 1e3) / 1e12,
+        "gemm_share": g_ms / sum(k["total_ms"] for k in ks),
+        "gemm_kernels": {k["name"]: {"TFLOP/s": k["flops"] / (k["total_ms"] / 1e3) / 1e12,
+                                     "ms_per_step": k["total_ms"] / 3} for k in gemm}}
+    del big, x, dy
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_e2e(fp, layers, cache, ws, ctx, N, dev, world, args, stream):
-    """Same step through the C ABI with inputs copied from pinned host memory
-    and outputs copied back inside the timed region."""
+    """Same step through the C ABI with every input copied from pinned host
+    memory and every result copied back inside the timed region.  Copies and
+    compute run on three streams: the host-to-device copies of linear i+1 and
+    the device-to-host copies of linear i-1 overlap the kernels of linear i
+    (per-linear device buffers; cross-step waits keep a buffer from being
+    overwritten while a previous step still reads it)."""
     import torch
     host = []
     h2d = d2h = 0
@@ -354,22 +457,39 @@ def run_e2e(fp, layers, cache, ws, ctx, N, dev, world, args, stream):
         host.append((hx, hw, hdy, hy, hdx, hdw))
         h2d += 2 * (hx.numel() + hw.numel() + hdy.numel())
         d2h += 2 * (hy.numel() + hdx.numel() + hdw.numel())
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    n = len(layers)
+    ev_in = [torch.cuda.Event() for _ in range(n)]     # inputs of linear i on the device
+    ev_done = [torch.cuda.Event() for _ in range(n)]   # kernels of linear i finished
+    ev_out = [torch.cuda.Event() for _ in range(n)]    # results of linear i on the host
+    for e in ev_done + ev_out:
+        e.record(stream)
     version = [10 ** 6]
 
     def step():
         cache.begin_cycle()
         version[0] += 1
-        for L, (hx, hw, hdy, hy, hdx, hdw) in zip(layers, host):
-            L["x"].copy_(hx, non_blocking=True)
-            L["w"].copy_(hw, non_blocking=True)
-            L["dy"].copy_(hdy, non_blocking=True)
-            cache.get(L["h"], version[0], True)
+        for i, (L, (hx, hw, hdy, hy, hdx, hdw)) in enumerate(zip(layers, host)):
+            s_in.wait_event(ev_done[i])          # previous step's kernels no longer read them
+            with torch.cuda.stream(s_in):
+                L["x"].copy_(hx, non_blocking=True)
+                L["w"].copy_(hw, non_blocking=True)
+                L["dy"].copy_(hdy, non_blocking=True)
+                ev_in[i].record(s_in)
+            stream.wait_event(ev_in[i])
+            stream.wait_event(ev_out[i])         # previous step's results have left the device
+            cache.get(L["h"], version[0], True, stream=stream)
             c = fp.LinearContext(ctx.ctx, N, L["K"])
-            fp.fp8_linear_fwd(L["x"], cache, L["h"], RECIPE, ws=ws, y=L["y"], ctx=c)
-            fp.fp8_linear_bwd(L["dy"], c, cache, L["h"], RECIPE, ws=ws, dx=L["dx"], dw=L["dw"])
-            hy.copy_(L["y"], non_blocking=True)
-            hdx.copy_(L["dx"], non_blocking=True)
-            hdw.copy_(L["dw"], non_blocking=True)
+            fp.fp8_linear_fwd(L["x"], cache, L["h"], RECIPE, ws=ws, y=L["y"], ctx=c, stream=stream)
+            fp.fp8_linear_bwd(L["dy"], c, cache, L["h"], RECIPE, ws=ws, dx=L["dx"], dw=L["dw"],
+                              stream=stream)
+            ev_done[i].record(stream)
+            s_out.wait_event(ev_done[i])
+            with torch.cuda.stream(s_out):
+                hy.copy_(L["y"], non_blocking=True)
+                hdx.copy_(L["dx"], non_blocking=True)
+                hdw.copy_(L["dw"], non_blocking=True)
+                ev_out[i].record(s_out)
 
     k = max(3, min(args.steps, 20))
     step()
@@ -378,15 +498,22 @@ def run_e2e(fp, layers, cache, ws, ctx, N, dev, world, args, stream):
     barrier(world)
     torch.cuda.synchronize()
     t0.record(stream)
+    s_in.wait_stream(stream)     # no copy of the timed steps starts before t0
+    s_out.wait_stream(stream)
     for _ in range(k):
         step()
+    # the region ends when the last results are on the host
+    for e in ev_out:
+        stream.wait_event(e)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     ms = reduce_max(t0.elapsed_time(t1), world, dev) / k
     value = world * len(SHAPES) * N / (ms / 1e3)
     return {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": k, "ms_per_step": ms}
+            "d2h_bytes_per_step": d2h, "steps": k, "ms_per_step": ms,
+            "copy_GBps": (h2d + d2h) / (ms / 1e3) / 1e9,
+            "overlap": "H2D / compute / D2H on three streams"}
 
 
 def main(argv=None):
@@ -396,6 +523,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-mlp", action="store_true",
+                    help="skip the MLP-level workloads reported beside the main line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

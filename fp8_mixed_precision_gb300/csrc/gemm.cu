@@ -56,7 +56,7 @@ struct Cfg {
   static constexpr int kStageB = BN * BK;
   static constexpr int kStageBytes = kStageA + kStageB;
   static constexpr int kAccBufs = (int)kTmemCols / BN;
-  static constexpr int kCtlBytes = 4096;
+  static constexpr int kCtlBytes = 8192;
   static constexpr int kStages =
       (kSmemBudget - 1024 - kOutBytes - kCtlBytes) / kStageBytes < kMaxStages
           ? (kSmemBudget - 1024 - kOutBytes - kCtlBytes) / kStageBytes
@@ -85,9 +85,9 @@ struct SmemCtl {
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
-  float bscale[kEpiWarps][64];
+  float bscale[kEpiWarps][128];
 };
-static_assert(sizeof(SmemCtl) <= 4096, "control block");
+static_assert(sizeof(SmemCtl) <= 8192, "control block");
 
 // Bounded wait on phase `parity` of `bar`; false on abort or timeout.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort) {
@@ -193,6 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NB = C::kAccBufs;
   constexpr int kHalf = BN / 2;           // columns per epilogue warp
   constexpr int kSlabs = kHalf / 64;      // 64-column slabs per epilogue warp per tile
+  constexpr int kChunks = kHalf / 32;    // 32-column TMEM loads per warp per K block
+  constexpr int kPre = 4;                 // K blocks of scales held ahead in registers
   static_assert(SCALING == FP8_SCALING_TENSOR || BN == 128, "block scaling uses 128-wide tiles");
 
   extern __shared__ uint8_t smem_raw[];
@@ -363,80 +365,82 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++nacc;
       } else {
-        uint64_t acc[32];  // 64 fp32 accumulators as packed pairs
+        uint64_t acc[kHalf / 2];  // kHalf fp32 accumulators as packed pairs
 #pragma unroll
-        for (int j = 0; j < 32; ++j) acc[j] = 0;
+        for (int j = 0; j < kHalf / 2; ++j) acc[j] = 0;
         const int64_t mrow = m < g.M ? m : g.M - 1;  // clamp for the scale read only
         const float *arow = g.a_sinv + mrow * g.lds_a;
-        // scales of the current K block, loaded one block ahead
-        float sa = arow[kb0], sb_t = 0.0f, sbl0 = 0.0f, sbl1 = 0.0f;
-        const int64_t n0 = colbase + lane, n1 = colbase + 32 + lane;
-        if (SCALING == FP8_SCALING_1x128_128x128) {
-          sb_t = g.b_sinv[(int64_t)tn * g.lds_b + kb0];
-        } else {
-          sbl0 = n0 < g.N ? g.b_sinv[n0 * g.lds_b + kb0] : 0.0f;
-          sbl1 = n1 < g.N ? g.b_sinv[n1 * g.lds_b + kb0] : 0.0f;
-        }
+        const float *bt = g.b_sinv + (colbase / 128) * g.lds_b;  // 128x128: this warp's column block
+        // Scales of K blocks kb .. kb+kPre-1 in a register ring (slot 0 = current):
+        // the loads are issued kPre blocks before their use, hiding their latency.
+        float ra[kPre], rb[kPre][kChunks];
+        auto load_scales = [&](int k, float &a, float (&b)[kChunks]) {
+          a = k < kb1 ? arow[k] : 0.0f;
+          if (SCALING == FP8_SCALING_1x128_128x128) {
+            b[0] = k < kb1 ? bt[k] : 0.0f;
+          } else {
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) {
+              const int64_t n = colbase + 32 * c + lane;
+              b[c] = (k < kb1 && n < g.N) ? g.b_sinv[n * g.lds_b + k] : 0.0f;
+            }
+          }
+        };
+#pragma unroll
+        for (int i = 0; i < kPre; ++i) load_scales(kb0 + i, ra[i], rb[i]);
         bool ok = true;
         for (int kb = kb0; kb < kb1; ++kb) {
           const uint32_t ab = nacc % NB, aph = (nacc / NB) & 1;
-          const float sa_cur = sa, sbt_cur = sb_t;
+          const float sa_cur = ra[0], sbt_cur = rb[0][0];
           if (SCALING == FP8_SCALING_1x128_1x128) {
             __syncwarp();
-            ctl->bscale[warp - 2][lane] = sbl0;
-            ctl->bscale[warp - 2][32 + lane] = sbl1;
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) ctl->bscale[warp - 2][32 * c + lane] = rb[0][c];
             __syncwarp();
           }
-          if (kb + 1 < kb1) {  // prefetch the next block's scales
-            sa = arow[kb + 1];
-            if (SCALING == FP8_SCALING_1x128_128x128) {
-              sb_t = g.b_sinv[(int64_t)tn * g.lds_b + kb + 1];
-            } else {
-              sbl0 = n0 < g.N ? g.b_sinv[n0 * g.lds_b + kb + 1] : 0.0f;
-              sbl1 = n1 < g.N ? g.b_sinv[n1 * g.lds_b + kb + 1] : 0.0f;
-            }
+#pragma unroll
+          for (int i = 0; i + 1 < kPre; ++i) {
+            ra[i] = ra[i + 1];
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) rb[i][c] = rb[i + 1][c];
           }
+          load_scales(kb + kPre, ra[kPre - 1], rb[kPre - 1]);
           if (!wait_bar(&ctl->acc_full[ab], aph, abort)) { ok = false; break; }
           ptx::tc_fence_after();
-          uint32_t raw0[32], raw1[32];
-          ptx::tmem_ld32(tl + ab * BN, raw0);
-          ptx::tmem_ld32(tl + ab * BN + 32, raw1);
-          ptx::tmem_ld_wait();
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty[ab]);
-          ++nacc;
-          if (SCALING == FP8_SCALING_1x128_128x128) {
-            const float s = __fmul_rn(sa_cur, sbt_cur);
-            const uint64_t s2 = pk(s, s);
+          const uint64_t sa2 = pk(sa_cur, sa_cur);
+          const uint64_t st2 = pk(__fmul_rn(sa_cur, sbt_cur), __fmul_rn(sa_cur, sbt_cur));
+          const uint64_t *bs = reinterpret_cast<const uint64_t *>(ctl->bscale[warp - 2]);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              acc[j] = fma2(pk(__uint_as_float(raw0[2 * j]), __uint_as_float(raw0[2 * j + 1])), s2,
-                            acc[j]);
-              acc[16 + j] = fma2(pk(__uint_as_float(raw1[2 * j]), __uint_as_float(raw1[2 * j + 1])),
-                                 s2, acc[16 + j]);
+          for (int c = 0; c < kChunks; ++c) {
+            uint32_t raw[32];
+            ptx::tmem_ld32(tl + ab * BN + 32 * c, raw);
+            ptx::tmem_ld_wait();
+            if (c == kChunks - 1) {  // the partial is in registers: free the TMEM buffer
+              ptx::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty[ab]);
             }
-          } else {
-            const uint64_t sa2 = pk(sa_cur, sa_cur);
-            const uint64_t *bs = reinterpret_cast<const uint64_t *>(ctl->bscale[warp - 2]);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const uint64_t s0 = mul2(sa2, bs[j]), s1 = mul2(sa2, bs[16 + j]);
-              acc[j] = fma2(pk(__uint_as_float(raw0[2 * j]), __uint_as_float(raw0[2 * j + 1])), s0,
-                            acc[j]);
-              acc[16 + j] = fma2(pk(__uint_as_float(raw1[2 * j]), __uint_as_float(raw1[2 * j + 1])),
-                                 s1, acc[16 + j]);
+              const uint64_t s2 = SCALING == FP8_SCALING_1x128_128x128 ? st2 : mul2(sa2, bs[16 * c + j]);
+              acc[16 * c + j] =
+                  fma2(pk(__uint_as_float(raw[2 * j]), __uint_as_float(raw[2 * j + 1])), s2,
+                       acc[16 * c + j]);
             }
           }
+          ++nacc;
         }
         if (!ok) break;
-        float v0[32], v1[32];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          upk(acc[j], v0[2 * j], v0[2 * j + 1]);
-          upk(acc[16 + j], v1[2 * j], v1[2 * j + 1]);
+        for (int s = 0; s < kSlabs; ++s) {
+          float v0[32], v1[32];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            upk(acc[32 * s + j], v0[2 * j], v0[2 * j + 1]);
+            upk(acc[32 * s + 16 + j], v1[2 * j], v1[2 * j + 1]);
+          }
+          emit(v0, v1, 1.0f, colbase + 64 * s, slab_y, split);
         }
-        emit(v0, v1, 1.0f, colbase, slab_y, split);
       }
     }
     if (!SPLIT && lane == 0) ptx::bulk_wait<0>();  // stores complete before the CTA exits
@@ -562,7 +566,7 @@ cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const C
   const int64_t grid = std::min<int64_t>(g.units, num_sms());
   // algorithmic bytes: FP8 operands once, bf16 output once, block scales
   double bytes = (double)g.M * g.K + (double)g.N * g.K + 2.0 * g.M * g.N;
-  if (SCALING == FP8_SCALING_1x128_128x128) bytes += 4.0 * g.kbs * (g.M + g.tiles_n);
+  if (SCALING == FP8_SCALING_1x128_128x128) bytes += 4.0 * g.kbs * (g.M + (g.N + 127) / 128);
   if (SCALING == FP8_SCALING_1x128_1x128) bytes += 4.0 * g.kbs * (g.M + g.N);
   LaunchScope ls(names[SCALING], st, bytes, 2.0 * g.M * g.N * g.K);
   fp8_gemm_kernel<SCALING, SPLIT, BN><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(ta, tb, tc,

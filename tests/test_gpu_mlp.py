@@ -1,0 +1,167 @@
+"""GPU parity of the MLP-level workloads: the block-scaled MLP block (fc1 ->
+GELU -> fc2, fwd + bwd), the weight cache under gradient accumulation in a
+stack (cached vs uncached bitwise identical, one weight quantization per
+cycle), and the large block-scaled linear with 1% x100 outliers checked on
+sampled output tiles at its full size."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as o
+from fp8_mixed_precision_gb300 import synthetic as syn
+from parity import assert_bytes_equal, assert_f32_equal, check_gemm, to_np
+
+pytestmark = pytest.mark.gpu
+
+REL_TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def fp():
+    from fp8_mixed_precision_gb300 import build
+    build.build()
+    import fp8_mixed_precision_gb300 as fp
+    return fp
+
+
+def _rel(got, exp_bits_or_f32):
+    g = o.bf16_to_f32(to_np(got)).astype(np.float64) if got.dtype == torch.bfloat16 \
+        else to_np(got).astype(np.float64)
+    e = exp_bits_or_f32
+    e = o.bf16_to_f32(e).astype(np.float64) if e.dtype == np.uint16 else e.astype(np.float64)
+    return float(np.linalg.norm(g - e) / max(np.linalg.norm(e), 1e-300))
+
+
+def _oracle_stack(xb, w1b, w2b, dyb, recipe):
+    """Oracle chain for a stack of MLP blocks, one microbatch."""
+    L = len(w1b)
+    w1q = [o.quantize(w, recipe, "weight") for w in w1b]
+    w2q = [o.quantize(w, recipe, "weight") for w in w2b]
+    h, saved = xb, []
+    for l in range(L):
+        f1 = o.linear_fwd(h, w1q[l], recipe)
+        a = o.gelu_fwd(f1["y"])
+        f2 = o.linear_fwd(a, w2q[l], recipe)
+        saved.append((f1, a, f2))
+        h = f2["y"]
+    y = h
+    g = dyb
+    dw1, dw2 = [None] * L, [None] * L
+    for l in reversed(range(L)):
+        f1, a, f2 = saved[l]
+        b2 = o.linear_bwd(g, f2, w2q[l], recipe)
+        dh = o.gelu_bwd(b2["dx"], f1["y"])
+        b1 = o.linear_bwd(dh, f1, w1q[l], recipe)
+        dw1[l], dw2[l] = b1["dw"], b2["dw"]
+        g = b1["dx"]
+    return dict(y=y, dx=g, dw1=dw1, dw2=dw2, h0=saved[0][0]["y"], xq0=saved[0][0]["xq"])
+
+
+@pytest.mark.parametrize("recipe", ["block", "tensorwise"])
+@pytest.mark.parametrize("N", [4096, 400])
+def test_mlp_block_parity(fp, recipe, N):
+    from fp8_mixed_precision_gb300.mlp import FP8MLPStack
+    d, ffn = 512, 2048
+    st = FP8MLPStack(d, ffn, 1, N, recipe)
+    x = syn.bf16_normal((N, d), 1.0, syn.SEED_X, device="cuda")
+    dy = syn.bf16_normal((N, d), 1e-3, syn.SEED_DY, device="cuda")
+    st.step([x], [dy], use_cache=True)
+    torch.cuda.synchronize()
+    assert fp.fp8_get_device_status() == 0
+    r = _oracle_stack(syn.bits(x), [syn.bits(st.w1[0])], [syn.bits(st.w2[0])], syn.bits(dy), recipe)
+    # first stage from synthetic inputs: bytes exact, fc1 output within the GEMM bound
+    xq_col = st.ctx1[0].ctx[:N * d].view(d, N)
+    assert_bytes_equal(xq_col, r["xq0"]["col"], "Xq colwise (fc1 context)")
+    xq = r["xq0"]
+    w1q = o.quantize(syn.bits(st.w1[0]), recipe, "weight")
+    A = o.dequantize(xq["row"], xq["row_scale_inv"], "e4m3")
+    B = o.dequantize(w1q["row"], w1q["row_scale_inv"], "e4m3")
+    check_gemm(st.H[0], A @ B.T, np.abs(A) @ np.abs(B).T, d, "H = fc1(X)")
+    # end to end (later stages see tolerance-matched inputs): relative Frobenius
+    rels = {"Y": _rel(st.Y[0], r["y"]), "dX": _rel(st.g[0], r["dx"]),
+            "dW1": _rel(st.dw1[0], o.bf16_to_f32(r["dw1"][0])),
+            "dW2": _rel(st.dw2[0], o.bf16_to_f32(r["dw2"][0]))}
+    for k, v in rels.items():
+        assert v <= REL_TOL, f"{k}: relative Frobenius error {v:.3g}"
+
+
+@pytest.mark.parametrize("recipe", ["block", "tensorwise"])
+def test_stack_weight_cache_bitwise(fp, recipe):
+    """Two-layer stack, GA = 4: is_first_microbatch True/False against None
+    gives bitwise identical outputs and accumulated gradients over two
+    cycles; the cached run quantizes each of the 4 weights once per cycle."""
+    from fp8_mixed_precision_gb300.mlp import FP8MLPStack
+    d, ffn, N, L, GA = 512, 2048, 1024, 2, 4
+    xs = [syn.bf16_normal((N, d), 1.0, 500 + i, device="cuda") for i in range(GA)]
+    dys = [syn.bf16_normal((N, d), 1e-3, 600 + i, device="cuda") for i in range(GA)]
+    res = {}
+    for use in (False, True):
+        st = FP8MLPStack(d, ffn, L, N, recipe)
+        n0 = fp.fp8_launch_count()
+        outs = [st.step(xs, dys, use) for _ in range(2)]
+        torch.cuda.synchronize()
+        res[use] = (outs, [t.clone() for t in st.dw1 + st.dw2], st.requantized,
+                    fp.fp8_launch_count() - n0)
+    (o_u, g_u, q_u, l_u), (o_c, g_c, q_c, l_c) = res[False], res[True]
+    assert q_u == 2 * GA * 2 * L and q_c == 2 * 2 * L
+    assert l_c < l_u
+    for cyc_u, cyc_c in zip(o_u, o_c):
+        for (y1, dx1), (y2, dx2) in zip(cyc_u, cyc_c):
+            assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+            assert torch.equal(dx1.view(torch.int16), dx2.view(torch.int16))
+    for a, b in zip(g_u, g_c):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    # and the accumulated gradients agree with the oracle's chain + fp32 accumulation
+    w1b = [syn.bits(w) for w in st.w1]      # the stack's synthetic weights (generator output)
+    w2b = [syn.bits(w) for w in st.w2]
+    acc1 = [np.zeros((ffn, d), np.float32) for _ in range(L)]
+    for i in range(GA):
+        r = _oracle_stack(syn.bits(xs[i]), w1b, w2b, syn.bits(dys[i]), recipe)
+        for l in range(L):
+            acc1[l] = o.grad_accumulate(acc1[l], r["dw1"][l])
+    for l in range(L):
+        rel = _rel(g_c[l], acc1[l])
+        assert rel <= REL_TOL, f"dW1[{l}] accumulated: relative Frobenius error {rel:.3g}"
+
+
+def test_large_block_linear_sampled_tiles(fp):
+    """fc1 of the large block-scaled MLP at full size (4096 -> 14336, 16384
+    tokens, 1% of X entries x100): GPU fwd + bwd, oracle on sampled tiles."""
+    N, K, O = 16384, 4096, 14336
+    x = syn.bf16_normal((N, K), 1.0, syn.SEED_X, device="cuda", outlier_frac=0.01)
+    w = syn.bf16_normal((O, K), 0.02, syn.SEED_W, device="cuda")
+    dy = syn.bf16_normal((N, O), 1e-3, syn.SEED_DY, device="cuda")
+    cache = fp.WeightCache()
+    h = cache.register(w, "block")
+    cache.begin_cycle()
+    cache.get(h, 0, True)
+    y, ctx = fp.fp8_linear_fwd(x, cache, h, "block")
+    dx, dw = fp.fp8_linear_bwd(dy, ctx, cache, h, "block")
+    torch.cuda.synchronize()
+    assert fp.fp8_get_device_status() == 0
+    xb, wb, dyb = syn.bits(x), syn.bits(w), syn.bits(dy)
+    wq = o.quantize_128x128(wb, "e4m3")
+    e = cache.entries[h]
+    assert_bytes_equal(e.row, wq["row"], "Wq row")
+    assert_bytes_equal(e.col, wq["col"], "Wq col")
+    assert_f32_equal(e.col_scale_inv, wq["col_scale_inv"], "Wq col scale_inv")
+    rng = np.random.default_rng(3)
+    sl = lambda t: slice(t * 128, (t + 1) * 128)
+    for _ in range(3):
+        tm, tn, tk = int(rng.integers(N // 128)), int(rng.integers(O // 128)), int(rng.integers(K // 128))
+        # Y tile: X rows of tile tm (1x128 blocks along K), W rows of tile tn
+        xq = o.quantize_1x128(np.ascontiguousarray(xb[sl(tm)]), "e4m3")
+        A = o.dequantize(xq["row"], xq["row_scale_inv"], "e4m3")
+        B = o.dequantize(wq["row"][sl(tn)], wq["row_scale_inv"][tn:tn + 1], "e4m3")
+        check_gemm(y[sl(tm), sl(tn)], A @ B.T, np.abs(A) @ np.abs(B).T, K, f"Y tile {tm},{tn}")
+        # dX tile: dY rows of tile tm (1x128 blocks along O), W^T rows of tile tk
+        gq = o.quantize_1x128(np.ascontiguousarray(dyb[sl(tm)]), "e5m2")
+        A = o.dequantize(gq["row"], gq["row_scale_inv"], "e5m2")
+        B = o.dequantize(wq["col"][sl(tk)], wq["col_scale_inv"][tk:tk + 1], "e4m3")
+        check_gemm(dx[sl(tm), sl(tk)], A @ B.T, np.abs(A) @ np.abs(B).T, O, f"dX tile {tm},{tk}")
+        # dW tile: dY columns of tile tn and X columns of tile tk, 1x128 blocks along tokens
+        gc = o.quantize_1x128(np.ascontiguousarray(dyb[:, sl(tn)]), "e5m2")
+        xc = o.quantize_1x128(np.ascontiguousarray(xb[:, sl(tk)]), "e4m3")
+        A = o.dequantize(gc["col"], gc["col_scale_inv"], "e5m2")
+        B = o.dequantize(xc["col"], xc["col_scale_inv"], "e4m3")
+        check_gemm(dw[sl(tn), sl(tk)], A @ B.T, np.abs(A) @ np.abs(B).T, N, f"dW tile {tn},{tk}")
