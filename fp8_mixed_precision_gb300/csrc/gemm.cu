@@ -193,9 +193,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NB = C::kAccBufs;
   constexpr int kHalf = BN / 2;           // columns per epilogue warp
   constexpr int kSlabs = kHalf / 64;      // 64-column slabs per epilogue warp per tile
-  constexpr int kChunks = kHalf / 32;    // 32-column TMEM loads per warp per K block
-  constexpr int kPre = 4;                 // K blocks of scales held ahead in registers
-  static_assert(SCALING == FP8_SCALING_TENSOR || BN == 128, "block scaling uses 128-wide tiles");
+  // block scaling: the partial is consumed in kCw-column TMEM loads (16 for
+  // 256-wide tiles, which keep 128 fp32 accumulators per thread in registers)
+  constexpr int kCw = BN == 256 ? 16 : 32;
+  constexpr int kChunks = kHalf / kCw;
+  constexpr int kBl = kHalf / 32;         // per-lane column scales (1x128 x 1x128)
+  constexpr int kPre = BN == 256 ? 2 : 4; // K blocks of scales held ahead in registers
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -373,14 +376,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float *bt = g.b_sinv + (colbase / 128) * g.lds_b;  // 128x128: this warp's column block
         // Scales of K blocks kb .. kb+kPre-1 in a register ring (slot 0 = current):
         // the loads are issued kPre blocks before their use, hiding their latency.
-        float ra[kPre], rb[kPre][kChunks];
-        auto load_scales = [&](int k, float &a, float (&b)[kChunks]) {
+        float ra[kPre], rb[kPre][kBl];
+        auto load_scales = [&](int k, float &a, float (&b)[kBl]) {
           a = k < kb1 ? arow[k] : 0.0f;
           if (SCALING == FP8_SCALING_1x128_128x128) {
             b[0] = k < kb1 ? bt[k] : 0.0f;
           } else {
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
+            for (int c = 0; c < kBl; ++c) {
               const int64_t n = colbase + 32 * c + lane;
               b[c] = (k < kb1 && n < g.N) ? g.b_sinv[n * g.lds_b + k] : 0.0f;
             }
@@ -395,14 +398,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (SCALING == FP8_SCALING_1x128_1x128) {
             __syncwarp();
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) ctl->bscale[warp - 2][32 * c + lane] = rb[0][c];
+            for (int c = 0; c < kBl; ++c) ctl->bscale[warp - 2][32 * c + lane] = rb[0][c];
             __syncwarp();
           }
 #pragma unroll
           for (int i = 0; i + 1 < kPre; ++i) {
             ra[i] = ra[i + 1];
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) rb[i][c] = rb[i + 1][c];
+            for (int c = 0; c < kBl; ++c) rb[i][c] = rb[i + 1][c];
           }
           load_scales(kb + kPre, ra[kPre - 1], rb[kPre - 1]);
           if (!wait_bar(&ctl->acc_full[ab], aph, abort)) { ok = false; break; }
@@ -412,8 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t *bs = reinterpret_cast<const uint64_t *>(ctl->bscale[warp - 2]);
 #pragma unroll
           for (int c = 0; c < kChunks; ++c) {
-            uint32_t raw[32];
-            ptx::tmem_ld32(tl + ab * BN + 32 * c, raw);
+            uint32_t raw[kCw];
+            if constexpr (kCw == 16) ptx::tmem_ld16(tl + ab * BN + kCw * c, raw);
+            else ptx::tmem_ld32(tl + ab * BN + kCw * c, raw);
             ptx::tmem_ld_wait();
             if (c == kChunks - 1) {  // the partial is in registers: free the TMEM buffer
               ptx::tc_fence_before();
@@ -421,11 +425,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty[ab]);
             }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const uint64_t s2 = SCALING == FP8_SCALING_1x128_128x128 ? st2 : mul2(sa2, bs[16 * c + j]);
-              acc[16 * c + j] =
-                  fma2(pk(__uint_as_float(raw[2 * j]), __uint_as_float(raw[2 * j + 1])), s2,
-                       acc[16 * c + j]);
+            for (int j = 0; j < kCw / 2; ++j) {
+              const int p = (kCw / 2) * c + j;  // accumulator pair index
+              const uint64_t s2 = SCALING == FP8_SCALING_1x128_128x128 ? st2 : mul2(sa2, bs[p]);
+              acc[p] = fma2(pk(__uint_as_float(raw[2 * j]), __uint_as_float(raw[2 * j + 1])), s2,
+                            acc[p]);
             }
           }
           ++nacc;
@@ -530,7 +534,9 @@ struct Plan {
 // Kernel configuration as a function of (M, N, K, scaling) only.
 Plan make_plan(int64_t M, int64_t N, int64_t K, int scaling) {
   Plan p;
-  p.bn = (scaling == FP8_SCALING_TENSOR && N >= 256) ? 256 : 128;
+  // 256-wide tiles halve the A re-reads and the per-SM operand traffic per
+  // flop; the 1x128 x 1x128 promotion needs per-column scales and stays 128-wide
+  p.bn = (N >= 256 && scaling != FP8_SCALING_1x128_1x128) ? 256 : 128;
   p.tiles_m = (int)((M + BM - 1) / BM);
   p.tiles_n = (int)((N + p.bn - 1) / p.bn);
   p.kbs = (int)((K + BK - 1) / BK);
@@ -577,7 +583,7 @@ cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const C
 template <int SCALING>
 cudaError_t launch_scaling(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
                            const GemmArgs &g, bool split, int bn, cudaStream_t st) {
-  if constexpr (SCALING == FP8_SCALING_TENSOR) {
+  if constexpr (SCALING != FP8_SCALING_1x128_1x128) {
     if (bn == 256)
       return split ? launch_variant<SCALING, true, 256>(ta, tb, tc, g, st)
                    : launch_variant<SCALING, false, 256>(ta, tb, tc, g, st);

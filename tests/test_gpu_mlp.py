@@ -13,7 +13,16 @@ from parity import assert_bytes_equal, assert_f32_equal, check_gemm, to_np
 
 pytestmark = pytest.mark.gpu
 
-REL_TOL = 2e-3
+REL_TOL = 2e-3   # relative Frobenius bound of one GEMM stage fed by exact (synthetic) inputs
+
+
+def chain_tol(stages: int) -> float:
+    """Bound for an output `stages` GEMMs away from the synthetic inputs.
+    Every stage after the first re-quantizes a bf16 input that is itself only
+    tolerance-matched to the oracle's, so a few FP8 codes (or a block scale)
+    may round differently; each stage adds at most its own 2e-3 to the
+    relative error it receives."""
+    return REL_TOL * stages
 
 
 @pytest.fixture(scope="module")
@@ -78,11 +87,13 @@ def test_mlp_block_parity(fp, recipe, N):
     B = o.dequantize(w1q["row"], w1q["row_scale_inv"], "e4m3")
     check_gemm(st.H[0], A @ B.T, np.abs(A) @ np.abs(B).T, d, "H = fc1(X)")
     # end to end (later stages see tolerance-matched inputs): relative Frobenius
-    rels = {"Y": _rel(st.Y[0], r["y"]), "dX": _rel(st.g[0], r["dx"]),
-            "dW1": _rel(st.dw1[0], o.bf16_to_f32(r["dw1"][0])),
-            "dW2": _rel(st.dw2[0], o.bf16_to_f32(r["dw2"][0]))}
-    for k, v in rels.items():
-        assert v <= REL_TOL, f"{k}: relative Frobenius error {v:.3g}"
+    # GEMM stages on the longest path from the synthetic inputs: Y = fc2(GELU(fc1 X)) 2;
+    # dX = fc1 dgrad of GELU'(fc1 X) * fc2 dgrad(dY) 2; dW1 = fc1 wgrad of that 3; dW2 2
+    rels = {"Y": (_rel(st.Y[0], r["y"]), 2), "dX": (_rel(st.g[0], r["dx"]), 2),
+            "dW1": (_rel(st.dw1[0], o.bf16_to_f32(r["dw1"][0])), 3),
+            "dW2": (_rel(st.dw2[0], o.bf16_to_f32(r["dw2"][0])), 2)}
+    for k, (v, n) in rels.items():
+        assert v <= chain_tol(n), f"{k}: relative Frobenius error {v:.3g} ({n} stages)"
 
 
 @pytest.mark.parametrize("recipe", ["block", "tensorwise"])
@@ -120,8 +131,11 @@ def test_stack_weight_cache_bitwise(fp, recipe):
         for l in range(L):
             acc1[l] = o.grad_accumulate(acc1[l], r["dw1"][l])
     for l in range(L):
+        # dW1[l]: 2 (L - 1 - l) dgrads through the later blocks, fc2(l) dgrad,
+        # then the wgrad -> 2 (L - l) stages
         rel = _rel(g_c[l], acc1[l])
-        assert rel <= REL_TOL, f"dW1[{l}] accumulated: relative Frobenius error {rel:.3g}"
+        n = 2 * (L - l)
+        assert rel <= chain_tol(n), f"dW1[{l}] accumulated: relative Frobenius error {rel:.3g}"
 
 
 def test_large_block_linear_sampled_tiles(fp):
