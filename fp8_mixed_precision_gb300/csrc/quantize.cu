@@ -8,19 +8,25 @@
 // post: blockwise, no amax history): 1x128 blocks for activations and
 // gradients, 128x128 tiles for weights.
 //
-// Work decomposition (all modes): one CTA of 256 threads owns a 128x128 tile.
-//   phase 1  thread t holds 16 consecutive columns (cg = t & 7) of 4 rows
-//            (rr = t >> 3, rows rr + 32 i): two 16-byte loads per row, the
-//            bf16 kept packed in registers.  Scales are formed, the rowwise
-//            bytes are stored with one 16-byte store per row (8 lanes = one
-//            128-byte row segment), and the bytes meant for the transposed
-//            layout go to a swizzled 16 KB shared-memory tile.
-//   phase 2  thread t reads a 16-row x 4-column byte block (16 conflict-free
-//            32-bit shared loads), transposes it in registers with byte
-//            permutes and writes 4 transposed rows of 16 bytes (8 lanes = one
-//            128-byte segment of a transposed row).
+// Work decomposition (all modes): persistent CTAs of 256 threads, one 128x128
+// bf16 tile per loop iteration, staged in shared memory by cp.async into two
+// buffers so the next tile's load overlaps the current tile's work.
+// Thread t owns 8 consecutive columns (cg = t & 15) of 8 rows (rr = t >> 4,
+// rows rr + 16 i): 16 lanes cover one 256-byte row, so every shared read is
+// conflict-free and every rowwise store is a contiguous 128-byte segment.
+//   maxima    one pass with packed bf16 |max| (128x128: the tile maximum;
+//             1x128: row maxima over the 16 lanes of a row, column maxima
+//             over the CTA), then one IEEE division per thread forms the 128
+//             row scales and the 128 column scales (tensorwise: the scale
+//             comes from the first pass's partial maxima)
+//   cast      packed fp32 multiplies, saturating RNE conversion; the rowwise
+//             bytes are stored, the bytes of the transposed layout go to a
+//             swizzled 16 KB tile
+//   transpose thread t reads a 16-row x 4-column byte block (conflict-free
+//             32-bit shared loads), transposes it with byte permutes and writes
+//             4 transposed rows of 16 bytes (8 lanes = one 128-byte segment)
 // Ragged tails: the last tile may have fewer rows/columns (multiples of 16);
-// absent elements are zeros for the amax and are never stored.
+// absent elements are zero-filled (zeros never raise an amax) and never stored.
 #include "common.cuh"
 #include "internal.h"
 
@@ -33,7 +39,7 @@ constexpr int kAmaxThreads = 512;
 
 // Word w (4 bytes = 4 columns) of tile row r lives at word index
 // r*32 + (w ^ swz(r)); swz keeps 4-word groups contiguous and makes the
-// phase-2 column reads hit 32 distinct banks.
+// transpose reads hit 32 distinct banks.
 __device__ __forceinline__ int swz(int r) { return ((r >> 4) & 7) << 2; }
 
 // ---------------------------------------------------------------------------
@@ -89,39 +95,107 @@ struct QParams {
   int n_partials;
 };
 
-// A product x * scale can only be NaN when x is inf or NaN (scale is finite
-// and non-negative; inf * 0 needs an infinite x), so a row slot whose 16
-// inputs are all finite converts without the NaN fix-up.
+struct __align__(16) QSmem {
+  uint16_t in[2][128 * 128];  // bf16 tiles, 256 bytes per row
+  uint32_t tile[128 * 32];    // FP8 bytes for the transposed layout (swizzled words)
+  float colred[8][128];       // 1x128: per-warp column maxima
+  float colsc[128];           // 1x128: column scales
+  float rowmx[128];           // 1x128: row maxima
+  float rowsc[128];           // 1x128: row scales
+  float red[8];
+  float tscale[2];
+};
+constexpr size_t kQSmemBytes = sizeof(QSmem);
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, bool valid) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait1() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+
+// Eight fp32 values -> eight FP8 bytes (two little-endian words).  A product
+// x * scale can only be NaN when x is inf or NaN (scale is finite and
+// non-negative), so `special` (some input non-finite) selects the NaN fix-up.
 template <int FMT>
-__device__ __forceinline__ uint4 cast16(const float (&v)[16], bool special) {
-  uint4 q;
+__device__ __forceinline__ uint2 cast8(const float (&v)[8], bool special) {
+  uint2 q;
   if (!special) {
     q.x = cvt4_finite<FMT>(v[0], v[1], v[2], v[3]);
     q.y = cvt4_finite<FMT>(v[4], v[5], v[6], v[7]);
-    q.z = cvt4_finite<FMT>(v[8], v[9], v[10], v[11]);
-    q.w = cvt4_finite<FMT>(v[12], v[13], v[14], v[15]);
   } else {
     q.x = cvt4<FMT>(v[0], v[1], v[2], v[3]);
     q.y = cvt4<FMT>(v[4], v[5], v[6], v[7]);
-    q.z = cvt4<FMT>(v[8], v[9], v[10], v[11]);
-    q.w = cvt4<FMT>(v[12], v[13], v[14], v[15]);
   }
   return q;
 }
 
+__device__ __forceinline__ bool nonfinite4(uint4 w) {
+  const uint32_t e = 0x7F807F80u;
+  return (__vcmpeq2(w.x & e, e) | __vcmpeq2(w.y & e, e) | __vcmpeq2(w.z & e, e) |
+          __vcmpeq2(w.w & e, e)) != 0;
+}
+
+// max(acc, |w|) on packed bf16 pairs; NaN lanes of w are ignored (max.bf16x2
+// returns the non-NaN operand).
+__device__ __forceinline__ uint32_t absmax2(uint32_t acc, uint32_t w) {
+  __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&acc);
+  __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162 *>(&w);
+  __nv_bfloat162 r = __hmax2(a, __habs2(b));
+  return *reinterpret_cast<uint32_t *>(&r);
+}
+// Larger of the two non-negative bf16 halves, as an fp32 value.
+__device__ __forceinline__ float bf16pair_max(uint32_t w) {
+  return __uint_as_float(max(w & 0xFFFFu, w >> 16) << 16);
+}
+
+// Packed fp32 pair multiply (two IEEE round-to-nearest products).
+__device__ __forceinline__ void mul2(float a0, float a1, float s0, float s1, float &r0, float &r1) {
+  uint64_t a, s, r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(s) : "f"(s0), "f"(s1));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(s));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(r));
+}
+
+__device__ __forceinline__ void unpack8(uint4 w, float (&v)[8]) {
+  v[0] = bf16lo(w.x); v[1] = bf16hi(w.x); v[2] = bf16lo(w.y); v[3] = bf16hi(w.y);
+  v[4] = bf16lo(w.z); v[5] = bf16hi(w.z); v[6] = bf16lo(w.w); v[7] = bf16hi(w.w);
+}
+
 template <int MODE, int FMT>
-__global__ void __launch_bounds__(kQThreads, MODE == 0 ? 4 : 2) quant_tile_kernel(QParams p) {
-  __shared__ __align__(16) uint32_t tile[128 * 32];   // FP8 bytes for the transposed layout
-  __shared__ float colred[8][128];                     // 1x128: per-warp column maxima
-  __shared__ __align__(16) float colsc[128];           // 1x128: column scales
-  __shared__ float red8[8];
-  __shared__ float tscale[2];
+__global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
+  extern __shared__ uint8_t q_smem_raw[];
+  QSmem &S = *reinterpret_cast<QSmem *>(q_smem_raw);
 
   const float fmax = (FMT == FP8_FORMAT_E4M3) ? kE4M3Max : kE5M2Max;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int cg = t & 7, rr = t >> 3;
+  const int cg = t & 15, rr = t >> 4;
   const int64_t tiles_r = (p.R + 127) / 128, tiles_c = (p.C + 127) / 128;
   const int64_t ntiles = tiles_r * tiles_c;
+
+  // stage tile `id` into buffer b (zero fill outside the tensor)
+  auto prefetch = [&](int64_t id, int b) {
+    if (id < ntiles) {
+      const int64_t tr = id / tiles_c, tc = id % tiles_c;
+      const int64_t r0 = tr * 128, c0 = tc * 128;
+      const bool col_ok = c0 + 8 * cg < p.C;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = rr + 16 * i;
+        const bool ok = col_ok && r0 + r < p.R;
+        const uint16_t *src = ok ? p.x + (r0 + r) * p.C + c0 + 8 * cg : p.x;
+        cp_async16(&S.in[b][r * 128 + 8 * cg], src, ok);
+      }
+    }
+    cp_async_commit();
+  };
 
   float ts = 1.0f, tsi = 1.0f;
   if (MODE == Q_TENSOR) {
@@ -129,174 +203,169 @@ __global__ void __launch_bounds__(kQThreads, MODE == 0 ? 4 : 2) quant_tile_kerne
     for (int k = t; k < p.n_partials; k += kQThreads) a = fmaxf(a, p.partials[k]);
 #pragma unroll
     for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    if (lane == 0) red8[warp] = a;
+    if (lane == 0) S.red[warp] = a;
     __syncthreads();
     if (t == 0) {
       float m = 0.0f;
-      for (int k = 0; k < 8; ++k) m = fmaxf(m, red8[k]);
+      for (int k = 0; k < 8; ++k) m = fmaxf(m, S.red[k]);
       float s, si;
       scale_from_amax(m, fmax, s, si);
-      tscale[0] = s;
-      tscale[1] = si;
+      S.tscale[0] = s;
+      S.tscale[1] = si;
       if (blockIdx.x == 0) {
         if (p.row_scale) { p.row_scale[0] = s; p.row_scale_inv[0] = si; }
         if (p.col_scale) { p.col_scale[0] = s; p.col_scale_inv[0] = si; }
       }
     }
     __syncthreads();
-    ts = tscale[0];
-    tsi = tscale[1];
+    ts = S.tscale[0];
+    tsi = S.tscale[1];
   }
   (void)tsi;
 
-  for (int64_t tile_id = blockIdx.x; tile_id < ntiles; tile_id += gridDim.x) {
-    const int64_t tr = tile_id / tiles_c, tc = tile_id % tiles_c;
+  const bool want_row = p.out_row != nullptr;
+  const bool want_col = p.out_col != nullptr;
+  int64_t id = blockIdx.x;
+  prefetch(id, 0);
+  prefetch(id + gridDim.x, 1);
+  for (int k = 0; id < ntiles; ++k, id += gridDim.x) {
+    const int b = k & 1;
+    const uint16_t *in = S.in[b];
+    const int64_t tr = id / tiles_c, tc = id % tiles_c;
     const int64_t r0 = tr * 128, c0 = tc * 128;
     const int rows_here = (int)(p.R - r0 < 128 ? p.R - r0 : 128);
     const int cols_here = (int)(p.C - c0 < 128 ? p.C - c0 : 128);
-    const bool col_ok = 16 * cg < cols_here;
+    const bool col_ok = 8 * cg < cols_here;
+    cp_async_wait1();
+    __syncthreads();  // this tile is in shared memory for every thread
 
-    // ---- load 4 rows x 16 columns, packed bf16
-    uint4 raw[4][2];
+    // ---- maxima: one pass over the tile with packed bf16 |max|
+    float s_tile = ts;
+    uint32_t cm[4] = {0, 0, 0, 0};  // column maxima of this thread's 8 columns (pairs)
+    if (MODE != Q_TENSOR) {
+      uint32_t tm = 0;              // 128x128: running tile maximum (pair)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = rr + 32 * i;
-      if (col_ok && r < rows_here) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.x + (r0 + r) * p.C + c0 + 16 * cg);
-        raw[i][0] = __ldcs(src);
-        raw[i][1] = __ldcs(src + 1);
+      for (int i = 0; i < 8; ++i) {
+        const int r = rr + 16 * i;
+        const uint4 w = *reinterpret_cast<const uint4 *>(&in[r * 128 + 8 * cg]);
+        if (MODE == Q_BLOCK1x128) {
+          cm[0] = absmax2(cm[0], w.x); cm[1] = absmax2(cm[1], w.y);
+          cm[2] = absmax2(cm[2], w.z); cm[3] = absmax2(cm[3], w.w);
+          uint32_t rm = absmax2(absmax2(absmax2(absmax2(0u, w.x), w.y), w.z), w.w);
+          float a = bf16pair_max(rm);
+#pragma unroll
+          for (int o = 1; o < 16; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+          if (cg == 0) S.rowmx[r] = a;
+        } else {
+          tm = absmax2(absmax2(absmax2(absmax2(tm, w.x), w.y), w.z), w.w);
+        }
+      }
+      if (MODE == Q_BLOCK128) {
+        float a = bf16pair_max(tm);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        if (lane == 0) S.red[warp] = a;
       } else {
-        raw[i][0] = make_uint4(0, 0, 0, 0);
-        raw[i][1] = make_uint4(0, 0, 0, 0);
+        // combine the two row groups of the warp, then store per-warp column maxima
+#pragma unroll
+        for (int j = 0; j < 4; ++j) cm[j] = absmax2(cm[j], __shfl_xor_sync(0xffffffffu, cm[j], 16));
+        if (lane < 16 && want_col) {
+          float4 *dst = reinterpret_cast<float4 *>(&S.colred[warp][8 * cg]);
+          dst[0] = make_float4(__uint_as_float(cm[0] << 16), __uint_as_float(cm[0] & 0xFFFF0000u),
+                               __uint_as_float(cm[1] << 16), __uint_as_float(cm[1] & 0xFFFF0000u));
+          dst[1] = make_float4(__uint_as_float(cm[2] << 16), __uint_as_float(cm[2] & 0xFFFF0000u),
+                               __uint_as_float(cm[3] << 16), __uint_as_float(cm[3] & 0xFFFF0000u));
+        }
       }
-    }
-    auto val = [&](int i, int j) -> float {  // element j (0..15) of row slot i
-      const uint4 &q = raw[i][j >> 3];
-      const uint32_t w = ((j & 7) < 2) ? q.x : ((j & 7) < 4) ? q.y : ((j & 7) < 6) ? q.z : q.w;
-      return (j & 1) ? bf16hi(w) : bf16lo(w);
-    };
-
-    // ---- scales
-    float rs[4], rsi[4];
-    if (MODE == Q_TENSOR) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) { rs[i] = ts; rsi[i] = tsi; }
-    } else if (MODE == Q_BLOCK128) {
-      float a = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 16; ++j) a = amax_acc(a, val(i, j));
-#pragma unroll
-      for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-      if (lane == 0) red8[warp] = a;
       __syncthreads();
-      float m = 0.0f;
+      if (MODE == Q_BLOCK128) {
+        float m = 0.0f;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) m = fmaxf(m, red8[k]);
-      float s, si;
-      scale_from_amax(m, fmax, s, si);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) { rs[i] = s; rsi[i] = si; }
-      if (t == 0) {
-        if (p.row_scale) {
-          p.row_scale[tr * tiles_c + tc] = s;
-          p.row_scale_inv[tr * tiles_c + tc] = si;
+        for (int w = 0; w < 8; ++w) m = fmaxf(m, S.red[w]);
+        float si;
+        scale_from_amax(m, fmax, s_tile, si);
+        if (t == 0) {
+          if (p.row_scale) {
+            p.row_scale[tr * tiles_c + tc] = s_tile;
+            p.row_scale_inv[tr * tiles_c + tc] = si;
+          }
+          if (p.col_scale) {
+            p.col_scale[tc * tiles_r + tr] = s_tile;
+            p.col_scale_inv[tc * tiles_r + tr] = si;
+          }
         }
-        if (p.col_scale) {
-          p.col_scale[tc * tiles_r + tr] = s;
-          p.col_scale_inv[tc * tiles_r + tr] = si;
-        }
-      }
-    } else {  // Q_BLOCK1x128
-      // row blocks: the 128 columns of a row are spread over the 8 lanes of one cg group
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float a = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) a = amax_acc(a, val(i, j));
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-        scale_from_amax(a, fmax, rs[i], rsi[i]);
-        const int r = rr + 32 * i;
-        if (cg == 0 && r < rows_here && p.out_row) {
-          p.row_scale[(r0 + r) * tiles_c + tc] = rs[i];
-          p.row_scale_inv[(r0 + r) * tiles_c + tc] = rsi[i];
-        }
-      }
-      if (p.out_col) {
-        // column blocks: 4 rows per thread, 4 row groups per warp (lane bits 3,4), 8 warps
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          float a = 0.0f;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) a = amax_acc(a, val(i, j));
-          a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
-          a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
-          if (lane < 8) colred[warp][16 * cg + j] = a;
-        }
-        __syncthreads();
+      } else {
+        // one division per thread: row scale of row t, column scale of column t
         if (t < 128) {
+          float s, si;
+          scale_from_amax(S.rowmx[t], fmax, s, si);
+          S.rowsc[t] = s;
+          if (want_row && t < rows_here) {
+            p.row_scale[(r0 + t) * tiles_c + tc] = s;
+            p.row_scale_inv[(r0 + t) * tiles_c + tc] = si;
+          }
+        } else if (want_col) {
+          const int c = t - 128;
           float m = 0.0f;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) m = fmaxf(m, colred[k][t]);
+          for (int w = 0; w < 8; ++w) m = fmaxf(m, S.colred[w][c]);
           float s, si;
           scale_from_amax(m, fmax, s, si);
-          colsc[t] = s;
-          if (t < cols_here) {
-            p.col_scale[(c0 + t) * tiles_r + tr] = s;
-            p.col_scale_inv[(c0 + t) * tiles_r + tr] = si;
+          S.colsc[c] = s;
+          if (c < cols_here) {
+            p.col_scale[(c0 + c) * tiles_r + tr] = s;
+            p.col_scale_inv[(c0 + c) * tiles_r + tr] = si;
           }
         }
         __syncthreads();
       }
     }
 
-    // ---- cast: rowwise bytes (and, for one-scale tiles, the transposed source)
-    float cs[16];
-    if (MODE == Q_BLOCK1x128 && p.out_col) {
-      const float4 *c4 = reinterpret_cast<const float4 *>(colsc + 16 * cg);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float4 f = c4[k];
-        cs[4 * k] = f.x; cs[4 * k + 1] = f.y; cs[4 * k + 2] = f.z; cs[4 * k + 3] = f.w;
-      }
+    // ---- cast: rowwise bytes and the source of the transposed layout
+    float cs[8];
+    if (MODE == Q_BLOCK1x128 && want_col) {
+      const float4 *c4 = reinterpret_cast<const float4 *>(&S.colsc[8 * cg]);
+      const float4 f0 = c4[0], f1 = c4[1];
+      cs[0] = f0.x; cs[1] = f0.y; cs[2] = f0.z; cs[3] = f0.w;
+      cs[4] = f1.x; cs[5] = f1.y; cs[6] = f1.z; cs[7] = f1.w;
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = rr + 32 * i;
-      const bool special = any_nonfinite_bf16(raw[i][0], raw[i][1]);
-      const bool need_row = p.out_row || (MODE != Q_BLOCK1x128 && p.out_col);
-      if (need_row) {
-        const float s = rs[i];
-        float v[16];
+    for (int i = 0; i < 8; ++i) {
+      const int r = rr + 16 * i;
+      const uint4 w = *reinterpret_cast<const uint4 *>(&in[r * 128 + 8 * cg]);
+      float v[8];
+      unpack8(w, v);
+      const bool special = nonfinite4(w);
+      const float s = MODE == Q_BLOCK1x128 ? S.rowsc[r] : s_tile;
+      if (want_row || (MODE != Q_BLOCK1x128 && want_col)) {
+        float y[8];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(val(i, j), s);
-        const uint4 q = cast16<FMT>(v, special);
-        if (p.out_row && col_ok && r < rows_here)
-          *reinterpret_cast<uint4 *>(p.out_row + (r0 + r) * p.C + c0 + 16 * cg) = q;
-        if (MODE != Q_BLOCK1x128 && p.out_col)
-          *reinterpret_cast<uint4 *>(&tile[r * 32 + ((4 * cg) ^ swz(r))]) = q;
+        for (int j = 0; j < 8; j += 2) mul2(v[j], v[j + 1], s, s, y[j], y[j + 1]);
+        const uint2 q = cast8<FMT>(y, special);
+        if (want_row && col_ok && r < rows_here)
+          *reinterpret_cast<uint2 *>(p.out_row + (r0 + r) * p.C + c0 + 8 * cg) = q;
+        if (MODE != Q_BLOCK1x128 && want_col)
+          *reinterpret_cast<uint2 *>(&S.tile[r * 32 + ((2 * cg) ^ swz(r))]) = q;
       }
-      if (MODE == Q_BLOCK1x128 && p.out_col) {
-        float v[16];
+      if (MODE == Q_BLOCK1x128 && want_col) {
+        float y[8];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(val(i, j), cs[j]);
-        *reinterpret_cast<uint4 *>(&tile[r * 32 + ((4 * cg) ^ swz(r))]) = cast16<FMT>(v, special);
+        for (int j = 0; j < 8; j += 2) mul2(v[j], v[j + 1], cs[j], cs[j + 1], y[j], y[j + 1]);
+        *reinterpret_cast<uint2 *>(&S.tile[r * 32 + ((2 * cg) ^ swz(r))]) = cast8<FMT>(y, special);
       }
     }
+    __syncthreads();  // tile complete; the bf16 buffer is free again
+    prefetch(id + 2 * (int64_t)gridDim.x, b);
 
     // ---- transposed layout
-    if (p.out_col) {
-      __syncthreads();
+    if (want_col) {
       const int seg = t & 7, w = t >> 3;  // rows seg*16..+15, columns 4w..4w+3
       if (4 * w < cols_here && 16 * seg < rows_here) {
         uint32_t a[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int r = seg * 16 + i;
-          a[i] = tile[r * 32 + (w ^ swz(r))];
+          a[i] = S.tile[r * 32 + (w ^ swz(r))];
         }
         uint32_t o[4][4];  // o[jj][g]: transposed row 4w+jj, word g (rows 4g..4g+3 of the segment)
 #pragma unroll
@@ -316,8 +385,8 @@ __global__ void __launch_bounds__(kQThreads, MODE == 0 ? 4 : 2) quant_tile_kerne
               make_uint4(o[jj][0], o[jj][1], o[jj][2], o[jj][3]);
       }
     }
-    __syncthreads();  // tile / colred / colsc reused by the next iteration
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");  // no copy in flight at exit
 }
 
 // ---------------------------------------------------------------------------
@@ -346,9 +415,19 @@ int tensorwise_partials_count(int64_t rows, int64_t cols) {
 template <int MODE, int FMT>
 static cudaError_t launch_tile(const QParams &p, cudaStream_t st) {
   static const char *names[3] = {"quant_cast_tensorwise", "quant_block_1x128", "quant_block_128x128"};
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(quant_tile_kernel<MODE, FMT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kQSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
   const int64_t tr = (p.R + 127) / 128, tc = (p.C + 127) / 128;
   const int64_t ntiles = tr * tc;
-  const int64_t grid = std::min<int64_t>(ntiles, (int64_t)num_sms() * 8);
+  const int64_t grid = std::min<int64_t>(ntiles, (int64_t)num_sms() * 2);
   // algorithmic bytes: bf16 read + one byte per written layout + scale arrays
   double bytes = 2.0 * p.R * p.C + (p.out_row ? 1.0 * p.R * p.C : 0.0) +
                  (p.out_col ? 1.0 * p.R * p.C : 0.0);
@@ -359,7 +438,7 @@ static cudaError_t launch_tile(const QParams &p, cudaStream_t st) {
   else
     bytes += 16.0;
   LaunchScope ls(names[MODE], st, bytes, 0.0);
-  quant_tile_kernel<MODE, FMT><<<(unsigned)grid, kQThreads, 0, st>>>(p);
+  quant_tile_kernel<MODE, FMT><<<(unsigned)grid, kQThreads, kQSmemBytes, st>>>(p);
   return cudaGetLastError();
 }
 
