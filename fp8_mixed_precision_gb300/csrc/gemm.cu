@@ -56,7 +56,7 @@ struct Cfg {
   static constexpr int kStageB = BN * BK;
   static constexpr int kStageBytes = kStageA + kStageB;
   static constexpr int kAccBufs = (int)kTmemCols / BN;
-  static constexpr int kCtlBytes = 8192;
+  static constexpr int kCtlBytes = 12288;
   static constexpr int kStages =
       (kSmemBudget - 1024 - kOutBytes - kCtlBytes) / kStageBytes < kMaxStages
           ? (kSmemBudget - 1024 - kOutBytes - kCtlBytes) / kStageBytes
@@ -77,6 +77,7 @@ struct GemmArgs {
   int64_t lds_a, lds_b;  // row strides (floats) of the block scale arrays
   void *out;             // bf16 C [M, N], or fp32 partials [splits, M, N]
   uint32_t idesc;
+  int vec4;              // scale rows are 16-byte aligned in groups of 4 K blocks
 };
 
 struct SmemCtl {
@@ -85,9 +86,9 @@ struct SmemCtl {
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
-  float bscale[kEpiWarps][128];
+  float bscale[kEpiWarps][256];  // 1x128 x 1x128: column scales of 4 K blocks x 64 columns
 };
-static_assert(sizeof(SmemCtl) <= 8192, "control block");
+static_assert(sizeof(SmemCtl) <= 12288, "control block");
 
 // Bounded wait on phase `parity` of `bar`; false on abort or timeout.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort) {
@@ -376,43 +377,95 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float *bt = g.b_sinv + (colbase / 128) * g.lds_b;  // 128x128: this warp's column block
         // Scales of K blocks kb .. kb+kPre-1 in a register ring (slot 0 = current):
         // the loads are issued kPre blocks before their use, hiding their latency.
+        bool ok = true;
+        if constexpr (SCALING == FP8_SCALING_1x128_1x128) {
+          // Scales move in groups of 4 K blocks: one 16-byte load per row (A)
+          // and per column (B) fetches a group; the column scales of the
+          // current group are staged in this warp's shared slice once.
+          auto ld4 = [&](const float *row, int k) -> float4 {
+            if (g.vec4 && k + 3 < kb1) return *reinterpret_cast<const float4 *>(row + k);
+            float4 r;
+            r.x = k < kb1 ? row[k] : 0.0f;
+            r.y = k + 1 < kb1 ? row[k + 1] : 0.0f;
+            r.z = k + 2 < kb1 ? row[k + 2] : 0.0f;
+            r.w = k + 3 < kb1 ? row[k + 3] : 0.0f;
+            return r;
+          };
+          const int64_t n0 = colbase + lane, n1 = colbase + 32 + lane;
+          const bool n0ok = n0 < g.N, n1ok = n1 < g.N;
+          const float *brow0 = g.b_sinv + (n0ok ? n0 : g.N - 1) * g.lds_b;
+          const float *brow1 = g.b_sinv + (n1ok ? n1 : g.N - 1) * g.lds_b;
+          float *bsw = ctl->bscale[warp - 2];
+          float4 a_cur = ld4(arow, kb0), b0_cur = ld4(brow0, kb0), b1_cur = ld4(brow1, kb0);
+          for (int g0 = kb0; ok && g0 < kb1; g0 += 4) {
+            const float4 a_nxt = ld4(arow, g0 + 4), b0_nxt = ld4(brow0, g0 + 4),
+                         b1_nxt = ld4(brow1, g0 + 4);
+            __syncwarp();
+            bsw[0 * 64 + lane] = n0ok ? b0_cur.x : 0.0f;
+            bsw[1 * 64 + lane] = n0ok ? b0_cur.y : 0.0f;
+            bsw[2 * 64 + lane] = n0ok ? b0_cur.z : 0.0f;
+            bsw[3 * 64 + lane] = n0ok ? b0_cur.w : 0.0f;
+            bsw[0 * 64 + 32 + lane] = n1ok ? b1_cur.x : 0.0f;
+            bsw[1 * 64 + 32 + lane] = n1ok ? b1_cur.y : 0.0f;
+            bsw[2 * 64 + 32 + lane] = n1ok ? b1_cur.z : 0.0f;
+            bsw[3 * 64 + 32 + lane] = n1ok ? b1_cur.w : 0.0f;
+            __syncwarp();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              if (g0 + kk >= kb1) break;
+              const uint32_t ab = nacc % NB, aph = (nacc / NB) & 1;
+              const float sa = kk == 0 ? a_cur.x : kk == 1 ? a_cur.y : kk == 2 ? a_cur.z : a_cur.w;
+              if (!wait_bar(&ctl->acc_full[ab], aph, abort)) { ok = false; break; }
+              ptx::tc_fence_after();
+              const uint64_t sa2 = pk(sa, sa);
+              const float4 *bq = reinterpret_cast<const float4 *>(bsw + kk * 64);
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {  // two 32-column TMEM chunks
+                uint32_t raw[32];
+                ptx::tmem_ld32(tl + ab * BN + 32 * c, raw);
+                ptx::tmem_ld_wait();
+                if (c == 1) {  // the partial is in registers: free the TMEM buffer
+                  ptx::tc_fence_before();
+                  __syncwarp();
+                  if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty[ab]);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float4 b4 = bq[8 * c + j];  // scales of columns 32c + 4j .. +3
+                  const uint64_t s0 = mul2(sa2, pk(b4.x, b4.y)), s1 = mul2(sa2, pk(b4.z, b4.w));
+                  const int p = 16 * c + 2 * j;
+                  acc[p] = fma2(pk(__uint_as_float(raw[4 * j]), __uint_as_float(raw[4 * j + 1])), s0,
+                                acc[p]);
+                  acc[p + 1] = fma2(pk(__uint_as_float(raw[4 * j + 2]), __uint_as_float(raw[4 * j + 3])),
+                                    s1, acc[p + 1]);
+                }
+              }
+              ++nacc;
+            }
+            a_cur = a_nxt;
+            b0_cur = b0_nxt;
+            b1_cur = b1_nxt;
+          }
+        } else {
         float ra[kPre], rb[kPre][kBl];
         auto load_scales = [&](int k, float &a, float (&b)[kBl]) {
           a = k < kb1 ? arow[k] : 0.0f;
-          if (SCALING == FP8_SCALING_1x128_128x128) {
-            b[0] = k < kb1 ? bt[k] : 0.0f;
-          } else {
-#pragma unroll
-            for (int c = 0; c < kBl; ++c) {
-              const int64_t n = colbase + 32 * c + lane;
-              b[c] = (k < kb1 && n < g.N) ? g.b_sinv[n * g.lds_b + k] : 0.0f;
-            }
-          }
+          b[0] = k < kb1 ? bt[k] : 0.0f;
         };
 #pragma unroll
         for (int i = 0; i < kPre; ++i) load_scales(kb0 + i, ra[i], rb[i]);
-        bool ok = true;
         for (int kb = kb0; kb < kb1; ++kb) {
           const uint32_t ab = nacc % NB, aph = (nacc / NB) & 1;
           const float sa_cur = ra[0], sbt_cur = rb[0][0];
-          if (SCALING == FP8_SCALING_1x128_1x128) {
-            __syncwarp();
-#pragma unroll
-            for (int c = 0; c < kBl; ++c) ctl->bscale[warp - 2][32 * c + lane] = rb[0][c];
-            __syncwarp();
-          }
 #pragma unroll
           for (int i = 0; i + 1 < kPre; ++i) {
             ra[i] = ra[i + 1];
-#pragma unroll
-            for (int c = 0; c < kBl; ++c) rb[i][c] = rb[i + 1][c];
+            rb[i][0] = rb[i + 1][0];
           }
           load_scales(kb + kPre, ra[kPre - 1], rb[kPre - 1]);
           if (!wait_bar(&ctl->acc_full[ab], aph, abort)) { ok = false; break; }
           ptx::tc_fence_after();
-          const uint64_t sa2 = pk(sa_cur, sa_cur);
           const uint64_t st2 = pk(__fmul_rn(sa_cur, sbt_cur), __fmul_rn(sa_cur, sbt_cur));
-          const uint64_t *bs = reinterpret_cast<const uint64_t *>(ctl->bscale[warp - 2]);
 #pragma unroll
           for (int c = 0; c < kChunks; ++c) {
             uint32_t raw[kCw];
@@ -427,12 +480,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < kCw / 2; ++j) {
               const int p = (kCw / 2) * c + j;  // accumulator pair index
-              const uint64_t s2 = SCALING == FP8_SCALING_1x128_128x128 ? st2 : mul2(sa2, bs[p]);
-              acc[p] = fma2(pk(__uint_as_float(raw[2 * j]), __uint_as_float(raw[2 * j + 1])), s2,
+              acc[p] = fma2(pk(__uint_as_float(raw[2 * j]), __uint_as_float(raw[2 * j + 1])), st2,
                             acc[p]);
             }
           }
           ++nacc;
+        }
         }
         if (!ok) break;
 #pragma unroll
@@ -549,6 +602,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int scaling) {
     s = std::max(s, 1);
   }
   p.kb_per_split = (p.kbs + s - 1) / s;
+  if (s > 1) p.kb_per_split = (p.kb_per_split + 3) / 4 * 4;  // splits start on 4-block groups
   p.splits = (p.kbs + p.kb_per_split - 1) / p.kb_per_split;
   return p;
 }
@@ -629,6 +683,8 @@ cudaError_t launch_gemm(const uint8_t *A, int a_fmt, const float *a_sinv, const 
   g.lds_b = p.kbs;
   g.out = p.splits > 1 ? ws : Cout;
   g.idesc = ptx::idesc_f8f6f4((uint32_t)a_fmt, (uint32_t)b_fmt, BM, (uint32_t)p.bn);
+  g.vec4 = (p.kbs % 4 == 0) && (reinterpret_cast<uintptr_t>(a_sinv) % 16 == 0) &&
+           (reinterpret_cast<uintptr_t>(b_sinv) % 16 == 0);
   const bool split = p.splits > 1;
   cudaError_t e;
   switch (scaling) {
