@@ -284,6 +284,7 @@ def run_ours(args):
         peaks_fp8 = fp8_peak
         lb = workloads["large_block_mlp_4096_14336"]
         lb["gemm_frac_of_fp8_peak"] = lb["gemm_tflops"] / peaks_fp8
+        workloads.update(run_plain_and_assay(fp, dev, stream))
 
     # ---- CPU baseline (rank 0, one GPU only)
     cpu = None
@@ -433,6 +434,120 @@ def run_mlp_workloads(fp, dev, stream):
                                      "ms_per_step": k["total_ms"] / 3} for k in gemm}}
     del big, x, dy
     torch.cuda.empty_cache()
+    return out
+
+
+def run_plain_and_assay(fp, dev, stream):
+    """Plain-FP8 arm against the fused path on the isolated-linear shapes, the
+    GEMM-only BF16/FP8 assay and memory accounting (the reconstruction's
+    isolated-linear table columns, exactness paragraph and component assay).
+      plain: every tensor quantized by two separate passes (rowwise-only, then
+             transposed-only), GEMMs through fp8_gemm; fused: fp8_linear_fwd/bwd.
+      assay: each linear's three GEMMs in FP8 (this library) vs bf16 cuBLAS
+             (torch.matmul, context), summed per shape like the page.
+      memory: saved-for-backward bytes and peak device memory of one fwd+bwd,
+             FP8 (this library) vs a bf16 linear (torch autograd, context)."""
+    import torch
+    from fp8_mixed_precision_gb300 import synthetic as syn
+    N = N_TOKENS
+    out = {"plain_vs_fused": {}, "gemm_assay": {}, "memory": {}}
+
+    def timed(fn, reps=5):
+        fn()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(reps):
+            fn()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / reps
+
+    for i, (K, O) in enumerate(SHAPES):
+        x, w, dy = syn.linear_inputs(N, K, O, device=dev, layer=i)
+        cache = fp.WeightCache()
+        h = cache.register(w, RECIPE)
+        ws = fp.linear_workspace(RECIPE, N, K, O, dev)
+        res = {}
+
+        def fused():
+            cache.begin_cycle()
+            cache.get(h, 0, True)
+            y, ctx = fp.fp8_linear_fwd(x, cache, h, RECIPE, ws=ws)
+            dx, dw = fp.fp8_linear_bwd(dy, ctx, cache, h, RECIPE, ws=ws)
+            res["fused"] = (y, dx, dw)
+
+        def plain():
+            wr = fp.fp8_quantize(w, RECIPE, "weight", rowwise=True, colwise=False)
+            wc = fp.fp8_quantize(w, RECIPE, "weight", rowwise=False, colwise=True)
+            xr = fp.fp8_quantize(x, RECIPE, "act", rowwise=True, colwise=False)
+            xc = fp.fp8_quantize(x, RECIPE, "act", rowwise=False, colwise=True)
+            y = fp.fp8_gemm(xr["row"], "e4m3", xr["row_scale_inv"], wr["row"], "e4m3",
+                            wr["row_scale_inv"], "tensor")
+            gr = fp.fp8_quantize(dy, RECIPE, "grad", rowwise=True, colwise=False)
+            gc = fp.fp8_quantize(dy, RECIPE, "grad", rowwise=False, colwise=True)
+            dx = fp.fp8_gemm(gr["row"], "e5m2", gr["row_scale_inv"], wc["col"], "e4m3",
+                             wr["row_scale_inv"], "tensor")
+            dw = fp.fp8_gemm(gc["col"], "e5m2", gr["row_scale_inv"], xc["col"], "e4m3",
+                             xr["row_scale_inv"], "tensor")
+            res["plain"] = (y, dx, dw)
+
+        ms_f, ms_p = timed(fused), timed(plain)
+        same = all(torch.equal(a.view(torch.int16), b.view(torch.int16))
+                   for a, b in zip(res["fused"], res["plain"]))
+        out["plain_vs_fused"][f"{K}->{O}"] = {"fused_ms": ms_f, "plain_ms": ms_p,
+                                              "fused_speedup": ms_p / ms_f,
+                                              "outputs_bitwise_equal": bool(same)}
+        # GEMM-only assay: the three GEMMs of the linear, FP8 vs bf16 cuBLAS
+        xq = fp.fp8_quantize(x, RECIPE, "act")
+        wq = fp.fp8_quantize(w, RECIPE, "weight")
+        gq = fp.fp8_quantize(dy, RECIPE, "grad")
+
+        def g8():
+            fp.fp8_gemm(xq["row"], "e4m3", xq["row_scale_inv"], wq["row"], "e4m3", wq["row_scale_inv"], "tensor")
+            fp.fp8_gemm(gq["row"], "e5m2", gq["row_scale_inv"], wq["col"], "e4m3", wq["row_scale_inv"], "tensor")
+            fp.fp8_gemm(gq["col"], "e5m2", gq["row_scale_inv"], xq["col"], "e4m3", xq["row_scale_inv"], "tensor")
+
+        def g16():
+            torch.matmul(x, w.t())
+            torch.matmul(dy, w)
+            torch.matmul(dy.t(), x)
+
+        ms8, ms16 = timed(g8), timed(g16)
+        out["gemm_assay"][f"{K}->{O}"] = {"fp8_ms": ms8, "bf16_cublas_ms": ms16,
+                                          "bf16_over_fp8": ms16 / ms8}
+        # memory: saved for backward and peak of one fwd+bwd
+        ctx_b = fp._ctx_bytes(RECIPE, N, K)
+        res.clear()
+        del xq, wq, gq
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        torch.cuda.reset_peak_memory_stats(dev)
+        base = torch.cuda.memory_allocated(dev)
+        fused()
+        torch.cuda.synchronize()
+        peak8 = torch.cuda.max_memory_allocated(dev) - base
+        torch.cuda.empty_cache()
+        torch.cuda.reset_peak_memory_stats(dev)
+        base = torch.cuda.memory_allocated(dev)
+        xr_ = x.detach().requires_grad_(True)
+        wr_ = w.detach().requires_grad_(True)
+        yb = torch.nn.functional.linear(xr_, wr_)
+        yb.backward(dy)
+        torch.cuda.synchronize()
+        peak16 = torch.cuda.max_memory_allocated(dev) - base
+        del yb, xr_, wr_
+        out["memory"][f"{K}->{O}"] = {"fp8_saved_bytes": ctx_b, "bf16_saved_bytes": 2 * N * K,
+                                      "fp8_peak_bytes": peak8, "bf16_peak_bytes": peak16}
+        del x, w, dy, cache, ws
+        torch.cuda.empty_cache()
+    mlp = [f"{k}->{o}" for k, o in SHAPES if k != o]
+    sq = [f"{k}->{o}" for k, o in SHAPES if k == o]
+    a = out["gemm_assay"]
+    out["gemm_assay"]["summed_bf16_over_fp8_mlp_shapes"] = (
+        sum(a[s]["bf16_cublas_ms"] for s in mlp) / sum(a[s]["fp8_ms"] for s in mlp))
+    out["gemm_assay"]["summed_bf16_over_fp8_square"] = (
+        sum(a[s]["bf16_cublas_ms"] for s in sq) / sum(a[s]["fp8_ms"] for s in sq))
     return out
 
 

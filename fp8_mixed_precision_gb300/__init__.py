@@ -64,6 +64,7 @@ _SIGS = {
     "fp8_grad_accumulate": (_c_int, [_c_p, _c_p, _c_i64, _c_p]),
     "fp8_get_device_status": (_c_int, [_c_p]),
     "fp8_profile_begin": (_c_int, []),
+    "fp8_debug_wait_timeout": (_c_int, [ctypes.c_uint64, _c_p]),
 }
 
 
@@ -360,3 +361,8 @@ def fp8_profile_end() -> list:
     return [dict(name=arr[i].name.decode(), launches=int(arr[i].launches),
                  total_ms=float(arr[i].total_ms), bytes=float(arr[i].bytes),
                  flops=float(arr[i].flops)) for i in range(min(n.value, cap))]
+
+
+def fp8_debug_wait_timeout(limit_ns: int, stream=None):
+    """Enqueue the bounded-wait probe (a wait that nothing satisfies)."""
+    _check(lib().fp8_debug_wait_timeout(int(limit_ns), _stream(stream)), "fp8_debug_wait_timeout")

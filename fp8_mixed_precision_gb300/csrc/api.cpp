@@ -494,6 +494,11 @@ fp8_status fp8_profile_end(fp8_kernel_stat *out, int cap, int *n) {
   return st;
 }
 
+fp8_status fp8_debug_wait_timeout(uint64_t limit_ns, fp8_stream_t stream) {
+  if (limit_ns == 0 || limit_ns > 1000000000ull) return FP8_ERR_INVALID_ARG;
+  return from_cuda(launch_wait_timeout_probe(limit_ns, cs(stream)));
+}
+
 fp8_status fp8_get_device_status(fp8_stream_t stream) {
   unsigned s = 0;
   if (gemm_read_status(&s, cs(stream)) != cudaSuccess) return FP8_ERR_CUDA;

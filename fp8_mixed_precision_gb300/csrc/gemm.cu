@@ -511,6 +511,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Failure-detection test hook: one warp initialises an mbarrier that nothing
+// will ever arrive at and waits on it with the same bounded wait the GEMM
+// uses, but with a caller-chosen limit; on expiry it records FP8_ERR_TIMEOUT
+// in the status word and returns.  No trap, no fault, the context stays usable.
+__global__ void wait_timeout_probe_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = ptx::globaltimer();
+    while (!ptx::mbar_try_wait(&bar, 0)) {
+      if (ptx::globaltimer() - t0 > limit_ns) {
+        atomicCAS(&g_gemm_status, 0u, (unsigned)FP8_ERR_TIMEOUT);
+        break;
+      }
+    }
+  }
+}
+
 // Fixed-order sum of the split-K partials, rounded once to bf16.
 __global__ void splitk_reduce_kernel(const float *__restrict__ ws, int splits, int64_t mn,
                                      __nv_bfloat16 *__restrict__ C) {
@@ -704,6 +726,12 @@ cudaError_t launch_gemm(const uint8_t *A, int a_fmt, const float *a_sinv, const 
   LaunchScope ls("gemm_splitk_reduce", st, 4.0 * p.splits * mn + 2.0 * mn, (double)p.splits * mn);
   splitk_reduce_kernel<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, st>>>(
       static_cast<const float *>(ws), p.splits, mn, static_cast<__nv_bfloat16 *>(Cout));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout_probe(uint64_t limit_ns, cudaStream_t st) {
+  LaunchScope ls("wait_timeout_probe", st, 0.0, 0.0);
+  wait_timeout_probe_kernel<<<1, 32, 0, st>>>(limit_ns);
   return cudaGetLastError();
 }
 

@@ -44,6 +44,8 @@ size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int scaling);
 cudaError_t launch_gemm(const uint8_t *A, int a_fmt, const float *a_sinv, const uint8_t *B,
                         int b_fmt, const float *b_sinv, int64_t M, int64_t N, int64_t K,
                         int scaling, void *C, void *ws, cudaStream_t st);
+// Launches the bounded-wait probe (a wait nobody satisfies; limit_ns <= 1 s).
+cudaError_t launch_wait_timeout_probe(uint64_t limit_ns, cudaStream_t st);
 // Reads and clears the GEMM kernels' device status word (0 = ok).
 cudaError_t gemm_read_status(unsigned *status, cudaStream_t st);
 

@@ -276,6 +276,13 @@ fp8_status fp8_quantize_tensorwise_noalloc(const void *x, int64_t rows, int64_t 
  * traps.  Also returns FP8_ERR_CUDA if the stream reports an error. */
 fp8_status fp8_get_device_status(fp8_stream_t stream);
 
+/* Failure-detection test hook: enqueues one kernel that waits, with the same
+ * bounded wait the GEMM uses, on a barrier nothing will ever complete; after
+ * limit_ns nanoseconds (1 .. 1e9) it records FP8_ERR_TIMEOUT in the device
+ * status word and returns (no trap; the context stays usable).  Read the
+ * outcome with fp8_get_device_status.  Errors: INVALID_ARG, CUDA. */
+fp8_status fp8_debug_wait_timeout(uint64_t limit_ns, fp8_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -119,3 +119,59 @@ def test_gelu_and_accumulate(fp):
         exp = o.grad_accumulate(exp, db)
     torch.cuda.synchronize()
     assert np.array_equal(to_np(acc).view(np.uint32), exp.view(np.uint32))
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(fp):
+    """A device-side wait that nothing satisfies gives up after its limit,
+    records FP8_ERR_TIMEOUT (read and cleared by fp8_get_device_status), and
+    the context keeps working: no trap, no fault, no hang."""
+    import time
+    t0 = time.perf_counter()
+    fp.fp8_debug_wait_timeout(50_000_000)          # 50 ms
+    assert fp.fp8_get_device_status() == 5          # FP8_ERR_TIMEOUT
+    assert time.perf_counter() - t0 < 5.0
+    assert fp.fp8_get_device_status() == 0          # cleared
+    with pytest.raises(fp.FP8Error):
+        fp.fp8_debug_wait_timeout(0)
+    # the context is still usable: a GEMM runs and agrees with an exact case
+    a = torch.full((128, 128), 0x38, dtype=torch.uint8, device="cuda")   # E4M3 1.0
+    one = torch.ones(1, device="cuda")
+    c = fp.fp8_gemm(a, "e4m3", one, a, "e4m3", one, "tensor")
+    torch.cuda.synchronize()
+    assert torch.all(c.float() == 128.0)
+    assert fp.fp8_get_device_status() == 0
+
+
+@pytest.mark.parametrize("recipe", ["tensorwise", "block"])
+def test_fused_equals_plain_fp8(fp, recipe):
+    """Exactness of the fused dual-layout path ("Native FP8 MLP reconstruction",
+    exactness paragraph: fused output/dX/dW equal plain FP8 exactly): the
+    plain arm quantizes every tensor in two separate passes (rowwise only,
+    then transposed only) and calls the GEMMs directly; all bytes, scales and
+    outputs equal the fused fp8_linear_fwd/bwd bit for bit."""
+    N, K, O = 1024, 512, 768
+    x, w, dy = syn.linear_inputs(N, K, O, device="cuda")
+    cache = fp.WeightCache()
+    h = cache.register(w, recipe)
+    cache.begin_cycle()
+    cache.get(h, 0, True)
+    y, ctx = fp.fp8_linear_fwd(x, cache, h, recipe)
+    dx, dw = fp.fp8_linear_bwd(dy, ctx, cache, h, recipe)
+    q = lambda t, role, r, c: fp.fp8_quantize(t, recipe, role, rowwise=r, colwise=c)
+    wr, wc = q(w, "weight", True, False), q(w, "weight", False, True)
+    xr, xc = q(x, "act", True, False), q(x, "act", False, True)
+    gr, gc = q(dy, "grad", True, False), q(dy, "grad", False, True)
+    e = cache.entries[h]
+    assert torch.equal(wr["row"], e.row) and torch.equal(wc["col"], e.col)
+    blk = recipe == "block"
+    y2 = fp.fp8_gemm(xr["row"], "e4m3", xr["row_scale_inv"], wr["row"], "e4m3", wr["row_scale_inv"],
+                     "1x128_128x128" if blk else "tensor")
+    dx2 = fp.fp8_gemm(gr["row"], "e5m2", gr["row_scale_inv"], wc["col"], "e4m3",
+                      wc["col_scale_inv"] if blk else wc["row_scale_inv"],
+                      "1x128_128x128" if blk else "tensor")
+    dw2 = fp.fp8_gemm(gc["col"], "e5m2", gc["col_scale_inv"] if blk else gc["row_scale_inv"],
+                      xc["col"], "e4m3", xc["col_scale_inv"] if blk else xc["row_scale_inv"],
+                      "1x128_1x128" if blk else "tensor")
+    torch.cuda.synchronize()
+    for a, b, name in ((y, y2, "Y"), (dx, dx2, "dX"), (dw, dw2, "dW")):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), name
