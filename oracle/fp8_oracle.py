@@ -277,6 +277,24 @@ def quantize_128x128(x_bits: np.ndarray, fmt: str) -> dict:
                 col_scale_inv=np.ascontiguousarray(si.T))
 
 
+def quantize_delayed(x_bits: np.ndarray, fmt: str, history: np.ndarray, step: int) -> dict:
+    """DelayedScaling (TE2852 opening post: DelayedScaling keeps amax_history
+    state; Float8BlockScaling does not).  Reading, margin 0: the scale comes
+    from the largest amax recorded in the history *before* this tensor is
+    seen, scale = fp32(fmax / max(history)) with the same special cases as
+    current scaling; the tensor is cast with it; then this tensor's own amax
+    is written into the ring at position step mod len(history)."""
+    hist = np.array(history, dtype=np.float32, copy=True)
+    s, s_inv = scale_from_amax(amax_of(hist), fmt)
+    xf = bf16_to_f32(x_bits)
+    q = cast(xf, s, fmt)
+    hist[int(step) % len(hist)] = amax_of(xf)
+    s1 = np.array([s], dtype=np.float32).reshape(1)
+    si1 = np.array([s_inv], dtype=np.float32).reshape(1)
+    return dict(row=q, col=np.ascontiguousarray(q.T), row_scale=s1, row_scale_inv=si1,
+                col_scale=s1.copy(), col_scale_inv=si1.copy(), history=hist)
+
+
 def quantize(x_bits: np.ndarray, recipe: str, role: str) -> dict:
     """Dispatch on recipe ('tensorwise' | 'block') and role ('act' | 'weight' | 'grad')."""
     fmt = ROLE_FORMAT[role]
@@ -360,13 +378,19 @@ class WeightCache:
     the first get() of a cycle and the FP8 copy is returned afterwards;
     without it every get() re-quantizes."""
 
-    def __init__(self, recipe: str):
+    def __init__(self, recipe: str, history_len: int = 16):
         self.recipe = recipe
         self.entries = {}
         self.quantize_calls = 0
+        self.history_len = history_len
 
     def register(self, name, w_bits):
-        self.entries[name] = dict(w=w_bits, q=None)
+        self.entries[name] = dict(w=w_bits, q=None,
+                                  history=np.zeros(self.history_len, np.float32), steps=0)
+
+    def update(self, name, w_bits):
+        """The bf16 weight changed (e.g. an optimizer step between cycles)."""
+        self.entries[name]["w"] = w_bits
 
     def begin_cycle(self):
         for e in self.entries.values():
@@ -375,7 +399,13 @@ class WeightCache:
     def get(self, name, use_cache: bool) -> dict:
         e = self.entries[name]
         if not use_cache or e["q"] is None:
-            e["q"] = quantize(e["w"], self.recipe, "weight")
+            if self.recipe == "delayed":
+                r = quantize_delayed(e["w"], E4M3, e["history"], e["steps"])
+                e["history"] = r["history"]
+                e["steps"] += 1
+                e["q"] = r
+            else:
+                e["q"] = quantize(e["w"], self.recipe, "weight")
             self.quantize_calls += 1
         return e["q"]
 

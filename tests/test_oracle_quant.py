@@ -162,3 +162,43 @@ def test_ragged_tail_blocks(R, C):
         assert np.array_equal(w["row"][r0:, c0:], t["row"])
         assert w["row_scale"][-1, -1] == t["row_scale"][0]
         assert np.array_equal(w["col"], w["row"].T)
+
+
+def test_delayed_scaling_pins():
+    x = _inputs(256, 128, 1.0, 31)
+    xf = o.bf16_to_f32(x)
+    cur = o.quantize_tensorwise(x, "e4m3")
+    # empty history: scale 1 (amax 0 rule); the tensor's amax lands at step % H
+    r = o.quantize_delayed(x, "e4m3", np.zeros(4, np.float32), 6)
+    assert r["row_scale"][0] == 1.0 and r["row_scale_inv"][0] == 1.0
+    assert np.array_equal(r["row"], o.encode(xf, "e4m3"))
+    assert list(r["history"]) == [0.0, 0.0, float(cur["amax"]), 0.0]
+    # a history whose maximum equals this tensor's amax reduces to current scaling
+    h = np.array([0.5, cur["amax"], 0.25], np.float32)
+    r = o.quantize_delayed(x, "e4m3", h, 1)
+    assert np.array_equal(r["row"], cur["row"]) and r["row_scale"][0] == cur["row_scale"][0]
+    # the scale follows the history's maximum, not the current tensor
+    h = np.array([float(cur["amax"]) * 4], np.float32)
+    r = o.quantize_delayed(x, "e4m3", h, 0)
+    assert r["row_scale"][0] == np.float32(448.0) / np.float32(float(cur["amax"]) * 4)
+    assert r["history"][0] == cur["amax"]
+    assert np.array_equal(r["col"], r["row"].T)
+
+
+def test_delayed_weight_cache_is_not_bitwise_neutral():
+    # With an amax history, re-quantizing the same weight inside a cycle uses
+    # a scale the cached copy never saw: the two runs differ (the TE
+    # documentation's warning), unlike the non-delayed recipes.
+    w = _inputs(256, 256, 0.02, 5)
+    outs = {}
+    for use in (False, True):
+        c = o.WeightCache("delayed", history_len=4)
+        c.register("w", w)
+        got = []
+        for cyc in range(2):
+            c.begin_cycle()
+            for mb in range(3):
+                got.append(c.get("w", use)["row"].copy())
+        outs[use] = got
+    assert not all(np.array_equal(a, b) for a, b in zip(outs[False], outs[True]))
+    assert np.array_equal(outs[False][0], outs[True][0])   # first quantization agrees
