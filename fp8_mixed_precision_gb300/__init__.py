@@ -19,12 +19,13 @@ __all__ = [
     "fp8_quantize", "fp8_scale_shape", "fp8_gemm", "fp8_linear_fwd", "fp8_linear_bwd",
     "fp8_gelu_fwd", "fp8_gelu_bwd", "fp8_grad_accumulate", "fp8_get_device_status",
     "fp8_launch_count", "fp8_profile_begin", "fp8_profile_end", "WeightCache", "LinearContext",
+    "fp8_quantize_delayed", "fp8_debug_wait_timeout",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8lin.so")
 
-RECIPE = {"tensorwise": 0, "block": 1}
+RECIPE = {"tensorwise": 0, "block": 1, "delayed": 2}
 ROLE = {"act": 0, "weight": 1, "grad": 2}
 FORMAT = {"e4m3": 0, "e5m2": 1}
 SCALING = {"tensor": 0, "1x128_128x128": 1, "1x128_1x128": 2}
@@ -65,6 +66,11 @@ _SIGS = {
     "fp8_get_device_status": (_c_int, [_c_p]),
     "fp8_profile_begin": (_c_int, []),
     "fp8_debug_wait_timeout": (_c_int, [ctypes.c_uint64, _c_p]),
+    "fp8_quantize_delayed": (_c_int, [_c_p, _c_i64, _c_i64, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p,
+                                      ctypes.c_int32, _c_i64, _c_p, _c_sz, _c_p]),
+    "fp8_weight_cache_register_delayed": (_c_int, [_c_p, _c_p, _c_i64, _c_i64, _c_p, _c_p, _c_p,
+                                                   _c_p, _c_p, ctypes.c_int32, _c_p, _c_sz,
+                                                   ctypes.POINTER(ctypes.c_int32)]),
 }
 
 
@@ -172,6 +178,27 @@ def fp8_quantize(x: torch.Tensor, recipe: str, role: str, rowwise: bool = True,
     return out
 
 
+def fp8_quantize_delayed(x: torch.Tensor, role: str, history: torch.Tensor, step: int,
+                         rowwise: bool = True, colwise: bool = True, stream=None) -> dict:
+    """DelayedScaling quantize: scale from max(history), then history[step %
+    len] = amax(x).  history: float32 CUDA tensor (updated in place)."""
+    _need_bf16_cuda(x, "x")
+    if history.dtype != torch.float32 or not history.is_cuda:
+        raise ValueError("history must be a float32 CUDA tensor")
+    R, C = x.shape
+    dev = x.device
+    out = dict(row=torch.empty((R, C), dtype=torch.uint8, device=dev) if rowwise else None,
+               col=torch.empty((C, R), dtype=torch.uint8, device=dev) if colwise else None,
+               scale=torch.empty(1, dtype=torch.float32, device=dev),
+               scale_inv=torch.empty(1, dtype=torch.float32, device=dev))
+    ws = _empty_bytes(_quant_ws_bytes("tensorwise", R, C), dev)
+    _check(lib().fp8_quantize_delayed(_ptr(x), R, C, ROLE[role], _ptr(out["row"]), _ptr(out["col"]),
+                                      _ptr(out["scale"]), _ptr(out["scale_inv"]), _ptr(history),
+                                      history.numel(), int(step), _ptr(ws), ws.numel(),
+                                      _stream(stream)), "fp8_quantize_delayed")
+    return out
+
+
 def fp8_gemm(a: torch.Tensor, a_fmt: str, a_scale_inv: torch.Tensor, b: torch.Tensor, b_fmt: str,
              b_scale_inv: torch.Tensor, scaling: str, out: torch.Tensor | None = None,
              stream=None) -> torch.Tensor:
@@ -203,6 +230,7 @@ class _Entry:
     col_scale: torch.Tensor
     col_scale_inv: torch.Tensor
     ws: torch.Tensor
+    history: torch.Tensor | None = None
 
 
 class WeightCache:
@@ -218,10 +246,26 @@ class WeightCache:
     def handle(self):
         return self._h
 
-    def register(self, w: torch.Tensor, recipe: str) -> int:
+    def register(self, w: torch.Tensor, recipe: str, history_len: int = 16) -> int:
         _need_bf16_cuda(w, "w")
         O, K = w.shape
         dev = w.device
+        if recipe == "delayed":
+            s = torch.empty(1, dtype=torch.float32, device=dev)
+            si = torch.empty(1, dtype=torch.float32, device=dev)
+            e = _Entry(w=w, recipe=recipe,
+                       row=torch.empty((O, K), dtype=torch.uint8, device=dev),
+                       col=torch.empty((K, O), dtype=torch.uint8, device=dev),
+                       row_scale=s, row_scale_inv=si, col_scale=s, col_scale_inv=si,
+                       ws=_empty_bytes(_quant_ws_bytes("tensorwise", O, K), dev),
+                       history=torch.zeros(history_len, dtype=torch.float32, device=dev))
+            out = ctypes.c_int32()
+            _check(lib().fp8_weight_cache_register_delayed(
+                self._h, _ptr(w), O, K, _ptr(e.row), _ptr(e.col), _ptr(s), _ptr(si),
+                _ptr(e.history), history_len, _ptr(e.ws), e.ws.numel(), ctypes.byref(out)),
+                "fp8_weight_cache_register_delayed")
+            self.entries.append(e)
+            return out.value
         rs = fp8_scale_shape(recipe, "weight", O, K, False)
         cs = fp8_scale_shape(recipe, "weight", O, K, True)
         e = _Entry(w=w, recipe=recipe,

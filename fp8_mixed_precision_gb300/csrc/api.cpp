@@ -78,11 +78,15 @@ int format_of(fp8_role role) { return role == FP8_ROLE_GRAD ? FP8_FORMAT_E5M2 : 
 
 // 0 tensorwise, 1 1x128, 2 128x128
 int qmode_of(fp8_recipe recipe, fp8_role role) {
-  if (recipe == FP8_RECIPE_TENSORWISE) return 0;
+  if (recipe != FP8_RECIPE_BLOCK) return 0;
   return role == FP8_ROLE_WEIGHT ? 2 : 1;
 }
 
 bool valid_recipe(int r) { return r == FP8_RECIPE_TENSORWISE || r == FP8_RECIPE_BLOCK; }
+// Recipes a linear layer / weight cache accepts (delayed scaling needs per-tensor state).
+bool valid_linear_recipe(int r) { return valid_recipe(r) || r == FP8_RECIPE_DELAYED; }
+// Activations and gradients of a delayed-scaling linear use current tensorwise scaling.
+fp8_recipe act_recipe(fp8_recipe r) { return r == FP8_RECIPE_DELAYED ? FP8_RECIPE_TENSORWISE : r; }
 bool valid_role(int r) { return r >= FP8_ROLE_ACT && r <= FP8_ROLE_GRAD; }
 
 fp8_status check_dims(int64_t a, int64_t b) {
@@ -135,7 +139,8 @@ uint64_t fp8_launch_count(void) { return g_launches.load(std::memory_order_relax
 
 fp8_status fp8_scale_shape(fp8_recipe recipe, fp8_role role, int64_t rows, int64_t cols,
                            int colwise, int64_t *srows, int64_t *scols) {
-  if (!srows || !scols || !valid_recipe(recipe) || !valid_role(role)) return FP8_ERR_INVALID_ARG;
+  if (!srows || !scols || !valid_linear_recipe(recipe) || !valid_role(role))
+    return FP8_ERR_INVALID_ARG;
   if (rows < 0 || cols < 0) return FP8_ERR_INVALID_ARG;
   const int mode = qmode_of(recipe, role);
   if (mode == 0) {
@@ -153,8 +158,8 @@ fp8_status fp8_scale_shape(fp8_recipe recipe, fp8_role role, int64_t rows, int64
 
 fp8_status fp8_quantize_workspace_size(fp8_recipe recipe, int64_t rows, int64_t cols,
                                        size_t *bytes) {
-  if (!bytes || !valid_recipe(recipe) || rows < 0 || cols < 0) return FP8_ERR_INVALID_ARG;
-  *bytes = recipe == FP8_RECIPE_TENSORWISE ? (size_t)kMaxPartials * sizeof(float) : 0;
+  if (!bytes || !valid_linear_recipe(recipe) || rows < 0 || cols < 0) return FP8_ERR_INVALID_ARG;
+  *bytes = recipe != FP8_RECIPE_BLOCK ? (size_t)kMaxPartials * sizeof(float) : 0;
   return FP8_OK;
 }
 
@@ -182,6 +187,29 @@ fp8_status fp8_quantize(const void *x, int64_t rows, int64_t cols, fp8_recipe re
   return from_cuda(launch_quantize(x, rows, cols, mode, format_of(role), rowwise_out, colwise_out,
                                    row_scale, row_scale_inv, col_scale, col_scale_inv,
                                    static_cast<float *>(workspace), cs(stream)));
+}
+
+fp8_status fp8_quantize_delayed(const void *x, int64_t rows, int64_t cols, fp8_role role,
+                                uint8_t *rowwise_out, uint8_t *colwise_out, float *scale,
+                                float *scale_inv, float *amax_history, int32_t history_len,
+                                int64_t step, void *workspace, size_t workspace_bytes,
+                                fp8_stream_t stream) {
+  if (!valid_role(role) || history_len <= 0 || history_len > 1 << 20 || step < 0)
+    return FP8_ERR_INVALID_ARG;
+  fp8_status st = check_dims(rows, cols);
+  if (st != FP8_OK) return st;
+  if (!rowwise_out && !colwise_out) return FP8_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return FP8_OK;
+  if (!x || !scale || !scale_inv || !amax_history) return FP8_ERR_INVALID_ARG;
+  if (!aligned16(x) || (rowwise_out && !aligned16(rowwise_out)) ||
+      (colwise_out && !aligned16(colwise_out)))
+    return FP8_ERR_ALIGN;
+  if (workspace_bytes < (size_t)kMaxPartials * sizeof(float) || !workspace)
+    return FP8_ERR_WORKSPACE;
+  return from_cuda(launch_quantize_delayed(x, rows, cols, format_of(role), rowwise_out,
+                                           colwise_out, scale, scale_inv, amax_history,
+                                           history_len, step, static_cast<float *>(workspace),
+                                           cs(stream)));
 }
 
 fp8_status fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, fp8_scaling scaling,
@@ -221,6 +249,9 @@ struct fp8_weight_cache {
     size_t ws_bytes;
     uint64_t cycle;    // cycle in which the FP8 copy was last made (0 = never)
     uint64_t version;  // caller's weight version at that time
+    float *hist;       // delayed scaling: amax history ring (caller-owned), else null
+    int32_t hist_len;
+    int64_t steps;     // delayed scaling: quantizations so far (ring position)
   };
   std::vector<Entry> entries;
   uint64_t cycle = 1;
@@ -249,10 +280,29 @@ fp8_status fp8_weight_cache_register(fp8_weight_cache *cache, const void *w, int
   size_t need = 0;
   fp8_quantize_workspace_size(recipe, O, K, &need);
   if (workspace_bytes < need || (need && !workspace)) return FP8_ERR_WORKSPACE;
-  fp8_weight_cache::Entry e{w, O, K, recipe, w_row, w_col, row_scale, row_scale_inv,
-                            col_scale, col_scale_inv, workspace, workspace_bytes, 0, 0};
+  fp8_weight_cache::Entry e{w,         O,          K,         recipe,        w_row,
+                            w_col,     row_scale,  row_scale_inv, col_scale, col_scale_inv,
+                            workspace, workspace_bytes, 0,     0,             nullptr,
+                            0,         0};
   cache->entries.push_back(e);
   *out = (fp8_weight_handle)(cache->entries.size() - 1);
+  return FP8_OK;
+}
+
+fp8_status fp8_weight_cache_register_delayed(fp8_weight_cache *cache, const void *w, int64_t O,
+                                             int64_t K, uint8_t *w_row, uint8_t *w_col,
+                                             float *scale, float *scale_inv, float *amax_history,
+                                             int32_t history_len, void *workspace,
+                                             size_t workspace_bytes, fp8_weight_handle *out) {
+  if (!amax_history || history_len <= 0 || history_len > 1 << 20) return FP8_ERR_INVALID_ARG;
+  fp8_status st = fp8_weight_cache_register(cache, w, O, K, FP8_RECIPE_TENSORWISE, w_row, w_col,
+                                            scale, scale_inv, scale, scale_inv, workspace,
+                                            workspace_bytes, out);
+  if (st != FP8_OK) return st;
+  auto &e = cache->entries[*out];
+  e.recipe = FP8_RECIPE_DELAYED;
+  e.hist = amax_history;
+  e.hist_len = history_len;
   return FP8_OK;
 }
 
@@ -271,9 +321,16 @@ fp8_status fp8_weight_cache_get(fp8_weight_cache *cache, fp8_weight_handle h, ui
     if (e.version != w_version) return FP8_ERR_STALE;
     return FP8_OK;  // is_first_microbatch=False: reuse the FP8 copy
   }
-  fp8_status st = fp8_quantize(e.w, e.O, e.K, e.recipe, FP8_ROLE_WEIGHT, e.w_row, e.w_col,
-                               e.row_scale, e.row_scale_inv, e.col_scale, e.col_scale_inv, e.ws,
-                               e.ws_bytes, stream);
+  fp8_status st;
+  if (e.recipe == FP8_RECIPE_DELAYED) {
+    st = fp8_quantize_delayed(e.w, e.O, e.K, FP8_ROLE_WEIGHT, e.w_row, e.w_col, e.row_scale,
+                              e.row_scale_inv, e.hist, e.hist_len, e.steps, e.ws, e.ws_bytes,
+                              stream);
+    if (st == FP8_OK) ++e.steps;
+  } else {
+    st = fp8_quantize(e.w, e.O, e.K, e.recipe, FP8_ROLE_WEIGHT, e.w_row, e.w_col, e.row_scale,
+                      e.row_scale_inv, e.col_scale, e.col_scale_inv, e.ws, e.ws_bytes, stream);
+  }
   if (st != FP8_OK) return st;
   e.cycle = cache->cycle;
   e.version = w_version;
@@ -288,6 +345,7 @@ struct CtxLayout {
   size_t xq_col, scale, scale_inv, total;
 };
 CtxLayout ctx_layout(fp8_recipe recipe, int64_t N, int64_t K) {
+  recipe = act_recipe(recipe);
   CtxLayout L;
   const int64_t ns = scale_elems(recipe, FP8_ROLE_ACT, N, K, 1);
   L.xq_col = 0;
@@ -298,13 +356,14 @@ CtxLayout ctx_layout(fp8_recipe recipe, int64_t N, int64_t K) {
 }
 
 fp8_scaling fwd_scaling(fp8_recipe r) {
-  return r == FP8_RECIPE_TENSORWISE ? FP8_SCALING_TENSOR : FP8_SCALING_1x128_128x128;
+  return r == FP8_RECIPE_BLOCK ? FP8_SCALING_1x128_128x128 : FP8_SCALING_TENSOR;
 }
 fp8_scaling wgrad_scaling(fp8_recipe r) {
-  return r == FP8_RECIPE_TENSORWISE ? FP8_SCALING_TENSOR : FP8_SCALING_1x128_1x128;
+  return r == FP8_RECIPE_BLOCK ? FP8_SCALING_1x128_1x128 : FP8_SCALING_TENSOR;
 }
 
 size_t fwd_ws(fp8_recipe r, int64_t N, int64_t K, int64_t O) {
+  r = act_recipe(r);
   const int64_t ns = scale_elems(r, FP8_ROLE_ACT, N, K, 0);
   size_t qws = 0;
   fp8_quantize_workspace_size(r, N, K, &qws);
@@ -312,6 +371,7 @@ size_t fwd_ws(fp8_recipe r, int64_t N, int64_t K, int64_t O) {
          align_up(gemm_workspace_bytes(N, O, K, fwd_scaling(r)));
 }
 size_t bwd_ws(fp8_recipe r, int64_t N, int64_t K, int64_t O) {
+  r = act_recipe(r);
   const int64_t nr = scale_elems(r, FP8_ROLE_GRAD, N, O, 0);
   const int64_t nc = scale_elems(r, FP8_ROLE_GRAD, N, O, 1);
   size_t qws = 0;
@@ -325,14 +385,15 @@ size_t bwd_ws(fp8_recipe r, int64_t N, int64_t K, int64_t O) {
 }  // namespace
 
 fp8_status fp8_linear_ctx_size(fp8_recipe recipe, int64_t N, int64_t K, size_t *bytes) {
-  if (!bytes || !valid_recipe(recipe) || N < 0 || K < 0) return FP8_ERR_INVALID_ARG;
+  if (!bytes || !valid_linear_recipe(recipe) || N < 0 || K < 0) return FP8_ERR_INVALID_ARG;
   *bytes = ctx_layout(recipe, N, K).total;
   return FP8_OK;
 }
 
 fp8_status fp8_linear_workspace_size(fp8_recipe recipe, int64_t N, int64_t K, int64_t O,
                                      size_t *bytes) {
-  if (!bytes || !valid_recipe(recipe) || N < 0 || K < 0 || O < 0) return FP8_ERR_INVALID_ARG;
+  if (!bytes || !valid_linear_recipe(recipe) || N < 0 || K < 0 || O < 0)
+    return FP8_ERR_INVALID_ARG;
   *bytes = std::max(fwd_ws(recipe, N, K, O), bwd_ws(recipe, N, K, O));
   return FP8_OK;
 }
@@ -340,10 +401,11 @@ fp8_status fp8_linear_workspace_size(fp8_recipe recipe, int64_t N, int64_t K, in
 fp8_status fp8_linear_fwd(const void *X, int64_t N, int64_t K, fp8_weight_cache *cache,
                           fp8_weight_handle h, fp8_recipe recipe, void *Y, void *ctx, void *ws,
                           size_t ws_bytes, fp8_stream_t stream) {
-  if (!cache || h < 0 || (size_t)h >= cache->entries.size() || !valid_recipe(recipe))
+  if (!cache || h < 0 || (size_t)h >= cache->entries.size() || !valid_linear_recipe(recipe))
     return FP8_ERR_INVALID_ARG;
   const auto &e = cache->entries[h];
   if (e.recipe != recipe || e.K != K) return FP8_ERR_INVALID_ARG;
+  const fp8_recipe ar = act_recipe(recipe);
   fp8_status st = check_dims(N, K);
   if (st != FP8_OK) return st;
   if (e.cycle != cache->cycle) return FP8_ERR_STALE;
@@ -354,16 +416,16 @@ fp8_status fp8_linear_fwd(const void *X, int64_t N, int64_t K, fp8_weight_cache 
   if (ws_bytes < fwd_ws(recipe, N, K, O)) return FP8_ERR_WORKSPACE;
   const CtxLayout L = ctx_layout(recipe, N, K);
   uint8_t *c = static_cast<uint8_t *>(ctx);
-  const int64_t ns = scale_elems(recipe, FP8_ROLE_ACT, N, K, 0);
+  const int64_t ns = scale_elems(ar, FP8_ROLE_ACT, N, K, 0);
   size_t qws = 0;
-  fp8_quantize_workspace_size(recipe, N, K, &qws);
+  fp8_quantize_workspace_size(ar, N, K, &qws);
   Carver w(ws);
   uint8_t *xq_row = w.take<uint8_t>((size_t)N * K);
   float *rs = w.take<float>((size_t)ns * 4);
   float *rsi = w.take<float>((size_t)ns * 4);
   float *part = w.take<float>(qws);
   void *gws = w.take<void>(gemm_workspace_bytes(N, O, K, fwd_scaling(recipe)));
-  st = fp8_quantize(X, N, K, recipe, FP8_ROLE_ACT, xq_row, c + L.xq_col, rs, rsi,
+  st = fp8_quantize(X, N, K, ar, FP8_ROLE_ACT, xq_row, c + L.xq_col, rs, rsi,
                     reinterpret_cast<float *>(c + L.scale), reinterpret_cast<float *>(c + L.scale_inv),
                     part, qws, stream);
   if (st != FP8_OK) return st;
@@ -375,10 +437,11 @@ fp8_status fp8_linear_fwd(const void *X, int64_t N, int64_t K, fp8_weight_cache 
 fp8_status fp8_linear_bwd(const void *dY, int64_t N, int64_t O, const void *ctx,
                           fp8_weight_cache *cache, fp8_weight_handle h, fp8_recipe recipe, void *dX,
                           void *dW, void *ws, size_t ws_bytes, fp8_stream_t stream) {
-  if (!cache || h < 0 || (size_t)h >= cache->entries.size() || !valid_recipe(recipe))
+  if (!cache || h < 0 || (size_t)h >= cache->entries.size() || !valid_linear_recipe(recipe))
     return FP8_ERR_INVALID_ARG;
   const auto &e = cache->entries[h];
   if (e.recipe != recipe || e.O != O) return FP8_ERR_INVALID_ARG;
+  const fp8_recipe ar = act_recipe(recipe);
   fp8_status st = check_dims(N, O);
   if (st != FP8_OK) return st;
   if (e.cycle != cache->cycle) return FP8_ERR_STALE;
@@ -391,10 +454,10 @@ fp8_status fp8_linear_bwd(const void *dY, int64_t N, int64_t O, const void *ctx,
   if (ws_bytes < bwd_ws(recipe, N, K, O)) return FP8_ERR_WORKSPACE;
   const CtxLayout L = ctx_layout(recipe, N, K);
   const uint8_t *c = static_cast<const uint8_t *>(ctx);
-  const int64_t nr = scale_elems(recipe, FP8_ROLE_GRAD, N, O, 0);
-  const int64_t nc = scale_elems(recipe, FP8_ROLE_GRAD, N, O, 1);
+  const int64_t nr = scale_elems(ar, FP8_ROLE_GRAD, N, O, 0);
+  const int64_t nc = scale_elems(ar, FP8_ROLE_GRAD, N, O, 1);
   size_t qws = 0;
-  fp8_quantize_workspace_size(recipe, N, O, &qws);
+  fp8_quantize_workspace_size(ar, N, O, &qws);
   const size_t gbytes = std::max(gemm_workspace_bytes(N, K, O, fwd_scaling(recipe)),
                                  gemm_workspace_bytes(O, K, N, wgrad_scaling(recipe)));
   Carver w(ws);
@@ -406,7 +469,7 @@ fp8_status fp8_linear_bwd(const void *dY, int64_t N, int64_t O, const void *ctx,
   float *gcsi = w.take<float>((size_t)nc * 4);
   float *part = w.take<float>(qws);
   void *gws = w.take<void>(gbytes);
-  st = fp8_quantize(dY, N, O, recipe, FP8_ROLE_GRAD, g_row, g_col, grs, grsi, gcs, gcsi, part, qws,
+  st = fp8_quantize(dY, N, O, ar, FP8_ROLE_GRAD, g_row, g_col, grs, grsi, gcs, gcsi, part, qws,
                     stream);
   if (st != FP8_OK) return st;
   if (dX) {

@@ -38,6 +38,13 @@ cudaError_t launch_quantize(const void *x, int64_t rows, int64_t cols, int mode,
                             float *row_scale_inv, float *col_scale, float *col_scale_inv,
                             float *partials, cudaStream_t st);
 
+// Delayed scaling: cast with the scale of the history's maximum, then write
+// this tensor's amax to hist[step % hist_len] (partials: >= 2 x SMs floats).
+cudaError_t launch_quantize_delayed(const void *x, int64_t rows, int64_t cols, int fmt,
+                                    uint8_t *out_row, uint8_t *out_col, float *scale,
+                                    float *scale_inv, float *hist, int hist_len, int64_t step,
+                                    float *partials, cudaStream_t st);
+
 // FP8 GEMM (tcgen05).  scaling: fp8_scaling.  ws may be null when
 // gemm_workspace_bytes() is 0.
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int scaling);

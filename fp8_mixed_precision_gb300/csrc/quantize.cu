@@ -93,6 +93,9 @@ struct QParams {
   float *col_scale, *col_scale_inv;
   const float *partials;  // tensorwise: per-CTA amax of pass 1
   int n_partials;
+  const float *hist;      // delayed: amax history ring (scale source) or null
+  int hist_len;
+  float *cur_partials;    // delayed: per-CTA amax of this tensor, written by the cast pass
 };
 
 struct __align__(16) QSmem {
@@ -200,7 +203,11 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
   float ts = 1.0f, tsi = 1.0f;
   if (MODE == Q_TENSOR) {
     float a = 0.0f;
-    for (int k = t; k < p.n_partials; k += kQThreads) a = fmaxf(a, p.partials[k]);
+    if (p.hist) {  // delayed scaling: the history's maximum, before this tensor
+      for (int k = t; k < p.hist_len; k += kQThreads) a = fmaxf(a, p.hist[k]);
+    } else {
+      for (int k = t; k < p.n_partials; k += kQThreads) a = fmaxf(a, p.partials[k]);
+    }
 #pragma unroll
     for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
     if (lane == 0) S.red[warp] = a;
@@ -225,6 +232,7 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
 
   const bool want_row = p.out_row != nullptr;
   const bool want_col = p.out_col != nullptr;
+  uint32_t cur_max = 0;  // delayed: running |max| of this CTA's tiles (bf16 pair)
   int64_t id = blockIdx.x;
   prefetch(id, 0);
   prefetch(id + gridDim.x, 1);
@@ -336,6 +344,8 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
       float v[8];
       unpack8(w, v);
       const bool special = nonfinite4(w);
+      if (MODE == Q_TENSOR && p.cur_partials)
+        cur_max = absmax2(absmax2(absmax2(absmax2(cur_max, w.x), w.y), w.z), w.w);
       const float s = MODE == Q_BLOCK1x128 ? S.rowsc[r] : s_tile;
       if (want_row || (MODE != Q_BLOCK1x128 && want_col)) {
         float y[8];
@@ -387,6 +397,38 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
     }
   }
   asm volatile("cp.async.wait_all;" ::: "memory");  // no copy in flight at exit
+  if (MODE == Q_TENSOR && p.cur_partials) {
+    float a = bf16pair_max(cur_max);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    __syncthreads();
+    if (lane == 0) S.red[warp] = a;
+    __syncthreads();
+    if (t == 0) {
+      float m = 0.0f;
+      for (int w = 0; w < 8; ++w) m = fmaxf(m, S.red[w]);
+      p.cur_partials[blockIdx.x] = m;
+    }
+  }
+}
+
+// Delayed scaling, after the cast pass: this tensor's amax (the maximum of
+// the per-CTA partials) enters the history ring at position step mod len.
+__global__ void delayed_history_update_kernel(const float *__restrict__ partials, int n,
+                                              float *__restrict__ hist, int hist_len,
+                                              int64_t step) {
+  __shared__ float red[8];
+  float a = 0.0f;
+  for (int k = threadIdx.x; k < n; k += blockDim.x) a = fmaxf(a, partials[k]);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = 0.0f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
+    hist[step % hist_len] = m;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -458,6 +500,9 @@ cudaError_t launch_quantize(const void *x, int64_t rows, int64_t cols, int mode,
   p.col_scale_inv = col_scale_inv;
   p.partials = partials;
   p.n_partials = 0;
+  p.hist = nullptr;
+  p.hist_len = 0;
+  p.cur_partials = nullptr;
   if (mode == Q_TENSOR) {
     const int g = tensorwise_partials_count(rows, cols);
     {
@@ -476,6 +521,35 @@ cudaError_t launch_quantize(const void *x, int64_t rows, int64_t cols, int mode,
                                   : launch_tile<Q_BLOCK1x128, FP8_FORMAT_E5M2>(p, st);
   return fmt == FP8_FORMAT_E4M3 ? launch_tile<Q_BLOCK128, FP8_FORMAT_E4M3>(p, st)
                                 : launch_tile<Q_BLOCK128, FP8_FORMAT_E5M2>(p, st);
+}
+
+cudaError_t launch_quantize_delayed(const void *x, int64_t rows, int64_t cols, int fmt,
+                                    uint8_t *out_row, uint8_t *out_col, float *scale,
+                                    float *scale_inv, float *hist, int hist_len, int64_t step,
+                                    float *partials, cudaStream_t st) {
+  QParams p;
+  p.x = static_cast<const uint16_t *>(x);
+  p.R = rows;
+  p.C = cols;
+  p.out_row = out_row;
+  p.out_col = out_col;
+  p.row_scale = scale;
+  p.row_scale_inv = scale_inv;
+  p.col_scale = nullptr;
+  p.col_scale_inv = nullptr;
+  p.partials = nullptr;
+  p.n_partials = 0;
+  p.hist = hist;
+  p.hist_len = hist_len;
+  p.cur_partials = partials;
+  const int64_t ntiles = ((rows + 127) / 128) * ((cols + 127) / 128);
+  const int grid = (int)std::min<int64_t>(ntiles, (int64_t)num_sms() * 2);
+  cudaError_t e = fmt == FP8_FORMAT_E4M3 ? launch_tile<Q_TENSOR, FP8_FORMAT_E4M3>(p, st)
+                                         : launch_tile<Q_TENSOR, FP8_FORMAT_E5M2>(p, st);
+  if (e != cudaSuccess) return e;
+  LaunchScope ls("quant_delayed_history", st, 4.0 * grid + 4.0, 0.0);
+  delayed_history_update_kernel<<<1, 256, 0, st>>>(partials, grid, hist, hist_len, step);
+  return cudaGetLastError();
 }
 
 }  // namespace fp8lin

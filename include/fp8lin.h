@@ -74,7 +74,12 @@ typedef enum {
   FP8_ERR_WORKSPACE = 8    /* workspace smaller than the size query returned */
 } fp8_status;
 
-typedef enum { FP8_RECIPE_TENSORWISE = 0, FP8_RECIPE_BLOCK = 1 } fp8_recipe;
+/* FP8_RECIPE_DELAYED: DelayedScaling (TransformerEngine issue #2852, opening
+ * post: amax_history state).  Quantization by fp8_quantize_delayed; in a
+ * weight cache via fp8_weight_cache_register_delayed; in fp8_linear_fwd/bwd
+ * the weight uses its cache entry's history while activations and gradients
+ * use current tensorwise scaling.  fp8_quantize itself rejects it. */
+typedef enum { FP8_RECIPE_TENSORWISE = 0, FP8_RECIPE_BLOCK = 1, FP8_RECIPE_DELAYED = 2 } fp8_recipe;
 
 /* Operand role: ACT and WEIGHT use E4M3, GRAD uses E5M2 (reconstruction,
  * implementation paragraph).  Under FP8_RECIPE_BLOCK, WEIGHT selects 128x128
@@ -122,6 +127,20 @@ fp8_status fp8_quantize(const void *x, int64_t rows, int64_t cols, fp8_recipe re
 
 fp8_status fp8_quantize_workspace_size(fp8_recipe recipe, int64_t rows, int64_t cols,
                                        size_t *bytes);
+
+/* fp8_quantize_delayed: DelayedScaling, margin 0 (one pass over x).
+ *   scale = fp32(fmax / max(amax_history[0 .. history_len-1])) with the scale
+ *   rule's special cases (an all-zero history gives scale 1); x is cast with
+ *   it into rowwise_out [rows, cols] and/or colwise_out [cols, rows]; then
+ *   amax(x) is written to amax_history[step % history_len].  scale and
+ *   scale_inv receive one float each.  amax_history is caller-owned device
+ *   memory (zeros before the first call); workspace as for tensorwise
+ *   fp8_quantize_workspace_size.  Errors: INVALID_ARG, SHAPE, ALIGN, WORKSPACE, CUDA. */
+fp8_status fp8_quantize_delayed(const void *x, int64_t rows, int64_t cols, fp8_role role,
+                                uint8_t *rowwise_out, uint8_t *colwise_out, float *scale,
+                                float *scale_inv, float *amax_history, int32_t history_len,
+                                int64_t step, void *workspace, size_t workspace_bytes,
+                                fp8_stream_t stream);
 
 /* Shape [srows, scols] of the scale array of a layout (colwise = 0 or 1). */
 fp8_status fp8_scale_shape(fp8_recipe recipe, fp8_role role, int64_t rows, int64_t cols,
@@ -178,6 +197,17 @@ fp8_status fp8_weight_cache_register(fp8_weight_cache *cache, const void *w, int
                                      uint8_t *w_col, float *row_scale, float *row_scale_inv,
                                      float *col_scale, float *col_scale_inv, void *workspace,
                                      size_t workspace_bytes, fp8_weight_handle *out);
+
+/* Register a weight under DelayedScaling: one tensorwise scale (scale,
+ * scale_inv: one float each, shared by both layouts) and a caller-owned
+ * amax_history ring of history_len floats (zeros initially).  Every
+ * quantization get() performs advances the ring by one position, so
+ * re-quantizing inside a cycle (use_cache = 0) is not bitwise neutral. */
+fp8_status fp8_weight_cache_register_delayed(fp8_weight_cache *cache, const void *w, int64_t O,
+                                             int64_t K, uint8_t *w_row, uint8_t *w_col,
+                                             float *scale, float *scale_inv, float *amax_history,
+                                             int32_t history_len, void *workspace,
+                                             size_t workspace_bytes, fp8_weight_handle *out);
 
 fp8_status fp8_weight_cache_begin_cycle(fp8_weight_cache *cache);
 
