@@ -403,19 +403,23 @@ def run_mlp_workloads(fp, dev, stream):
     del stk, xs, dys, res, grads
     torch.cuda.empty_cache()
 
-    # ---- block MLP d=512, ffn=2048, 131072 tokens (one microbatch, fwd + bwd)
-    blk = FP8MLPStack(512, 2048, 1, 131072, "block", device=dev)
+    # ---- block MLP d=512, ffn=2048, 131072 tokens (one microbatch, fwd + bwd),
+    # unfused and with quantization fused into the GELU producers
     x = syn.bf16_normal((131072, 512), 1.0, syn.SEED_X, device=dev)
     dy = syn.bf16_normal((131072, 512), 1e-3, syn.SEED_DY, device=dev)
-    blk.step([x], [dy], True, keep_outputs=False)
-    ms = timed(lambda: blk.step([x], [dy], True, keep_outputs=False), 5)
-    out["block_mlp_512_2048"] = {"ms_per_step": ms, "tokens_per_s": 131072 / (ms / 1e3),
-                                 "tflops": 6 * 2 * 131072 * 512 * 2048 / (ms / 1e3) / 1e12}
-    del blk, x, dy
-    torch.cuda.empty_cache()
+    for fused in (False, True):
+        blk = FP8MLPStack(512, 2048, 1, 131072, "block", device=dev, fused=fused)
+        blk.step([x], [dy], True, keep_outputs=False)
+        ms = timed(lambda: blk.step([x], [dy], True, keep_outputs=False), 5)
+        out["block_mlp_512_2048" + ("_fused" if fused else "")] = {
+            "ms_per_step": ms, "tokens_per_s": 131072 / (ms / 1e3),
+            "tflops": 6 * 2 * 131072 * 512 * 2048 / (ms / 1e3) / 1e12}
+        del blk
+        torch.cuda.empty_cache()
+    del x, dy
 
     # ---- large block MLP d=4096, ffn=14336, 16384 tokens, 1% x100 outliers
-    big = FP8MLPStack(4096, 14336, 1, 16384, "block", device=dev)
+    big = FP8MLPStack(4096, 14336, 1, 16384, "block", device=dev, fused=True)
     x = syn.bf16_normal((16384, 4096), 1.0, syn.SEED_X, device=dev, outlier_frac=0.01)
     dy = syn.bf16_normal((16384, 4096), 1e-3, syn.SEED_DY, device=dev)
     big.step([x], [dy], True, keep_outputs=False)
@@ -427,6 +431,7 @@ def run_mlp_workloads(fp, dev, stream):
     g_ms = sum(k["total_ms"] for k in gemm)
     g_fl = sum(k["flops"] for k in gemm)
     out["large_block_mlp_4096_14336"] = {
+        "fused_producers": True,
         "ms_per_step": ms, "tokens_per_s": 16384 / (ms / 1e3),
         "gemm_tflops": g_fl / (g_ms / 1e3) / 1e12,
         "gemm_share": g_ms / sum(k["total_ms"] for k in ks),

@@ -71,6 +71,16 @@ _SIGS = {
     "fp8_weight_cache_register_delayed": (_c_int, [_c_p, _c_p, _c_i64, _c_i64, _c_p, _c_p, _c_p,
                                                    _c_p, _c_p, ctypes.c_int32, _c_p, _c_sz,
                                                    ctypes.POINTER(ctypes.c_int32)]),
+    "fp8_gelu_quantize": (_c_int, [_c_p, _c_i64, _c_i64, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p,
+                                   _c_p, _c_p]),
+    "fp8_gelu_bwd_quantize": (_c_int, [_c_p, _c_p, _c_i64, _c_i64, _c_int, _c_p, _c_p, _c_p, _c_p,
+                                       _c_p, _c_p, _c_p]),
+    "fp8_linear_ctx_layout": (_c_int, [_c_int, _c_i64, _c_i64, _c_p, ctypes.POINTER(_c_p),
+                                       ctypes.POINTER(_c_p), ctypes.POINTER(_c_p)]),
+    "fp8_linear_fwd_quantized": (_c_int, [_c_p, _c_p, _c_i64, _c_i64, _c_p, ctypes.c_int32, _c_int,
+                                          _c_p, _c_p, _c_sz, _c_p]),
+    "fp8_linear_bwd_quantized": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_p, _c_p,
+                                          ctypes.c_int32, _c_int, _c_p, _c_p, _c_p, _c_sz, _c_p]),
 }
 
 
@@ -410,3 +420,73 @@ def fp8_profile_end() -> list:
 def fp8_debug_wait_timeout(limit_ns: int, stream=None):
     """Enqueue the bounded-wait probe (a wait that nothing satisfies)."""
     _check(lib().fp8_debug_wait_timeout(int(limit_ns), _stream(stream)), "fp8_debug_wait_timeout")
+
+
+class QuantizedTensor:
+    """Caller-owned FP8 buffers of one [R, C] tensor under the block recipe:
+    row [R, C] + row scales, and the transposed layout, either owned here or
+    placed inside a linear context (col_ptrs from fp8_linear_ctx_layout)."""
+
+    def __init__(self, R: int, C: int, role: str, device, col_ptrs=None):
+        self.R, self.C = R, C
+        rs = fp8_scale_shape("block", role, R, C, False)
+        cs = fp8_scale_shape("block", role, R, C, True)
+        self.row = torch.empty((R, C), dtype=torch.uint8, device=device)
+        self.row_scale = torch.empty(rs, dtype=torch.float32, device=device)
+        self.row_scale_inv = torch.empty(rs, dtype=torch.float32, device=device)
+        if col_ptrs is None:
+            self.col = torch.empty((C, R), dtype=torch.uint8, device=device)
+            self.col_scale = torch.empty(cs, dtype=torch.float32, device=device)
+            self.col_scale_inv = torch.empty(cs, dtype=torch.float32, device=device)
+            self.col_ptrs = (_ptr(self.col), _ptr(self.col_scale), _ptr(self.col_scale_inv))
+        else:
+            self.col = self.col_scale = self.col_scale_inv = None
+            self.col_ptrs = col_ptrs
+
+
+def fp8_linear_ctx_layout(recipe: str, ctx: LinearContext):
+    """Device pointers of the transposed FP8 input and its scales inside ctx."""
+    a, b_, c = _c_p(), _c_p(), _c_p()
+    _check(lib().fp8_linear_ctx_layout(RECIPE[recipe], ctx.N, ctx.K, _ptr(ctx.ctx), ctypes.byref(a),
+                                       ctypes.byref(b_), ctypes.byref(c)), "fp8_linear_ctx_layout")
+    return (a, b_, c)
+
+
+def fp8_gelu_quantize(h: torch.Tensor, q: QuantizedTensor, recipe: str = "block", stream=None):
+    """q <- 1x128 E4M3 quantization of bf16(GELU(h)); the bf16 GELU output is not written."""
+    _need_bf16_cuda(h, "h")
+    R, C = h.shape
+    _check(lib().fp8_gelu_quantize(_ptr(h), R, C, RECIPE[recipe], _ptr(q.row), q.col_ptrs[0],
+                                   _ptr(q.row_scale), _ptr(q.row_scale_inv), q.col_ptrs[1],
+                                   q.col_ptrs[2], _stream(stream)), "fp8_gelu_quantize")
+    return q
+
+
+def fp8_gelu_bwd_quantize(da: torch.Tensor, h: torch.Tensor, q: QuantizedTensor,
+                          recipe: str = "block", stream=None):
+    """q <- 1x128 E5M2 quantization of bf16(dA * GELU'(H)); dH is not written."""
+    _need_bf16_cuda(da, "da")
+    _need_bf16_cuda(h, "h")
+    R, C = h.shape
+    _check(lib().fp8_gelu_bwd_quantize(_ptr(da), _ptr(h), R, C, RECIPE[recipe], _ptr(q.row),
+                                       q.col_ptrs[0], _ptr(q.row_scale), _ptr(q.row_scale_inv),
+                                       q.col_ptrs[1], q.col_ptrs[2], _stream(stream)),
+           "fp8_gelu_bwd_quantize")
+    return q
+
+
+def fp8_linear_fwd_quantized(xq: QuantizedTensor, cache: WeightCache, h: int, recipe: str,
+                             ws: torch.Tensor, y: torch.Tensor, stream=None):
+    _check(lib().fp8_linear_fwd_quantized(_ptr(xq.row), _ptr(xq.row_scale_inv), xq.R, xq.C,
+                                          cache.handle, h, RECIPE[recipe], _ptr(y), _ptr(ws),
+                                          ws.numel(), _stream(stream)), "fp8_linear_fwd_quantized")
+    return y
+
+
+def fp8_linear_bwd_quantized(gq: QuantizedTensor, ctx: LinearContext, cache: WeightCache, h: int,
+                             recipe: str, ws: torch.Tensor, dx, dw: torch.Tensor, stream=None):
+    _check(lib().fp8_linear_bwd_quantized(_ptr(gq.row), _ptr(gq.row_scale_inv), gq.col_ptrs[0],
+                                          gq.col_ptrs[2], gq.R, gq.C, _ptr(ctx.ctx), cache.handle,
+                                          h, RECIPE[recipe], _ptr(dx), _ptr(dw), _ptr(ws),
+                                          ws.numel(), _stream(stream)), "fp8_linear_bwd_quantized")
+    return dx, dw

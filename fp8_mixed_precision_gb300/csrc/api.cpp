@@ -482,6 +482,111 @@ fp8_status fp8_linear_bwd(const void *dY, int64_t N, int64_t O, const void *ctx,
                   dW, gws, gbytes, stream);
 }
 
+// ---------------------------------------------------------------- fused producers
+namespace {
+fp8_status check_block_outputs(const void *x, int64_t rows, int64_t cols, fp8_recipe recipe,
+                               uint8_t *row, uint8_t *col, float *rs, float *rsi, float *cs,
+                               float *csi) {
+  if (recipe != FP8_RECIPE_BLOCK) return FP8_ERR_UNSUPPORTED;
+  fp8_status st = check_dims(rows, cols);
+  if (st != FP8_OK) return st;
+  if (!row && !col) return FP8_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return FP8_OK;
+  if (!x || (row && (!rs || !rsi)) || (col && (!cs || !csi))) return FP8_ERR_INVALID_ARG;
+  if (!aligned16(x) || (row && !aligned16(row)) || (col && !aligned16(col))) return FP8_ERR_ALIGN;
+  return FP8_OK;
+}
+}  // namespace
+
+fp8_status fp8_gelu_quantize(const void *H, int64_t rows, int64_t cols, fp8_recipe recipe,
+                             uint8_t *rowwise_out, uint8_t *colwise_out, float *row_scale,
+                             float *row_scale_inv, float *col_scale, float *col_scale_inv,
+                             fp8_stream_t stream) {
+  fp8_status st = check_block_outputs(H, rows, cols, recipe, rowwise_out, colwise_out, row_scale,
+                                      row_scale_inv, col_scale, col_scale_inv);
+  if (st != FP8_OK || rows == 0 || cols == 0) return st;
+  return from_cuda(launch_gelu_quantize(H, nullptr, rows, cols, 0, rowwise_out, colwise_out,
+                                        row_scale, row_scale_inv, col_scale, col_scale_inv,
+                                        cs(stream)));
+}
+
+fp8_status fp8_gelu_bwd_quantize(const void *dA, const void *H, int64_t rows, int64_t cols,
+                                 fp8_recipe recipe, uint8_t *rowwise_out, uint8_t *colwise_out,
+                                 float *row_scale, float *row_scale_inv, float *col_scale,
+                                 float *col_scale_inv, fp8_stream_t stream) {
+  fp8_status st = check_block_outputs(dA, rows, cols, recipe, rowwise_out, colwise_out, row_scale,
+                                      row_scale_inv, col_scale, col_scale_inv);
+  if (st != FP8_OK || rows == 0 || cols == 0) return st;
+  if (!H) return FP8_ERR_INVALID_ARG;
+  if (!aligned16(H)) return FP8_ERR_ALIGN;
+  return from_cuda(launch_gelu_quantize(dA, H, rows, cols, 1, rowwise_out, colwise_out,
+                                        row_scale, row_scale_inv, col_scale, col_scale_inv,
+                                        cs(stream)));
+}
+
+fp8_status fp8_linear_ctx_layout(fp8_recipe recipe, int64_t N, int64_t K, void *ctx,
+                                 uint8_t **xq_col, float **col_scale, float **col_scale_inv) {
+  if (!valid_linear_recipe(recipe) || N < 0 || K < 0 || !ctx || !xq_col || !col_scale ||
+      !col_scale_inv)
+    return FP8_ERR_INVALID_ARG;
+  const CtxLayout L = ctx_layout(recipe, N, K);
+  uint8_t *c = static_cast<uint8_t *>(ctx);
+  *xq_col = c + L.xq_col;
+  *col_scale = reinterpret_cast<float *>(c + L.scale);
+  *col_scale_inv = reinterpret_cast<float *>(c + L.scale_inv);
+  return FP8_OK;
+}
+
+fp8_status fp8_linear_fwd_quantized(const uint8_t *xq_row, const float *xq_row_scale_inv,
+                                    int64_t N, int64_t K, fp8_weight_cache *cache,
+                                    fp8_weight_handle h, fp8_recipe recipe, void *Y, void *ws,
+                                    size_t ws_bytes, fp8_stream_t stream) {
+  if (!cache || h < 0 || (size_t)h >= cache->entries.size() || !valid_linear_recipe(recipe))
+    return FP8_ERR_INVALID_ARG;
+  const auto &e = cache->entries[h];
+  if (e.recipe != recipe || e.K != K) return FP8_ERR_INVALID_ARG;
+  fp8_status st = check_dims(N, K);
+  if (st != FP8_OK) return st;
+  if (e.cycle != cache->cycle) return FP8_ERR_STALE;
+  if (N == 0) return FP8_OK;
+  if (!xq_row || !xq_row_scale_inv || !Y || !ws) return FP8_ERR_INVALID_ARG;
+  const size_t g = gemm_workspace_bytes(N, e.O, K, fwd_scaling(recipe));
+  if (ws_bytes < g) return FP8_ERR_WORKSPACE;
+  return fp8_gemm(xq_row, FP8_FORMAT_E4M3, xq_row_scale_inv, e.w_row, FP8_FORMAT_E4M3,
+                  e.row_scale_inv, N, e.O, K, fwd_scaling(recipe), Y, ws, ws_bytes, stream);
+}
+
+fp8_status fp8_linear_bwd_quantized(const uint8_t *gq_row, const float *gq_row_scale_inv,
+                                    const uint8_t *gq_col, const float *gq_col_scale_inv,
+                                    int64_t N, int64_t O, const void *ctx, fp8_weight_cache *cache,
+                                    fp8_weight_handle h, fp8_recipe recipe, void *dX, void *dW,
+                                    void *ws, size_t ws_bytes, fp8_stream_t stream) {
+  if (!cache || h < 0 || (size_t)h >= cache->entries.size() || !valid_linear_recipe(recipe))
+    return FP8_ERR_INVALID_ARG;
+  const auto &e = cache->entries[h];
+  if (e.recipe != recipe || e.O != O) return FP8_ERR_INVALID_ARG;
+  fp8_status st = check_dims(N, O);
+  if (st != FP8_OK) return st;
+  if (e.cycle != cache->cycle) return FP8_ERR_STALE;
+  const int64_t K = e.K;
+  if (N == 0) return FP8_OK;
+  if (!gq_col || !gq_col_scale_inv || !ctx || !dW || !ws || (dX && (!gq_row || !gq_row_scale_inv)))
+    return FP8_ERR_INVALID_ARG;
+  const size_t gbytes = std::max(gemm_workspace_bytes(N, K, O, fwd_scaling(recipe)),
+                                 gemm_workspace_bytes(O, K, N, wgrad_scaling(recipe)));
+  if (ws_bytes < gbytes) return FP8_ERR_WORKSPACE;
+  const CtxLayout L = ctx_layout(recipe, N, K);
+  const uint8_t *c = static_cast<const uint8_t *>(ctx);
+  if (dX) {
+    st = fp8_gemm(gq_row, FP8_FORMAT_E5M2, gq_row_scale_inv, e.w_col, FP8_FORMAT_E4M3,
+                  e.col_scale_inv, N, K, O, fwd_scaling(recipe), dX, ws, ws_bytes, stream);
+    if (st != FP8_OK) return st;
+  }
+  return fp8_gemm(gq_col, FP8_FORMAT_E5M2, gq_col_scale_inv, c + L.xq_col, FP8_FORMAT_E4M3,
+                  reinterpret_cast<const float *>(c + L.scale_inv), O, K, N,
+                  wgrad_scaling(recipe), dW, ws, ws_bytes, stream);
+}
+
 // ---------------------------------------------------------------- glue + status
 fp8_status fp8_gelu_fwd(const void *H, void *A, int64_t n, fp8_stream_t stream) {
   if (n < 0) return FP8_ERR_INVALID_ARG;

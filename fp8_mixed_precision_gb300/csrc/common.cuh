@@ -79,6 +79,22 @@ __device__ __forceinline__ bool any_nonfinite_bf16(uint4 a, uint4 b) {
   return m != 0;
 }
 
+// Exact-erf GELU and its derivative in fp32 (shared by the standalone GELU
+// kernels and the fused GELU + quantize path, so both round identically).
+// Phi(h) via erfc keeps full relative precision for large negative h.
+__device__ __forceinline__ float gelu_f(float h) {
+  return 0.5f * h * erfcf(-h * 0.70710678118654752f);
+}
+__device__ __forceinline__ float gelu_grad_f(float h) {
+  const float cdf = 0.5f * erfcf(-h * 0.70710678118654752f);
+  const float pdf = expf(-0.5f * h * h) * 0.39894228040143268f;
+  return fmaf(h, pdf, cdf);
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

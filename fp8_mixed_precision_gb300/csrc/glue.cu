@@ -11,20 +11,8 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// Phi(h) via erfc, accurate for large negative h (no 1 + erf cancellation).
-__device__ __forceinline__ float gelu_f(float h) {
-  return 0.5f * h * erfcf(-h * 0.70710678118654752f);
-}
-__device__ __forceinline__ float gelu_grad_f(float h) {
-  const float cdf = 0.5f * erfcf(-h * 0.70710678118654752f);
-  const float pdf = expf(-0.5f * h * h) * 0.39894228040143268f;
-  return fmaf(h, pdf, cdf);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t *>(&v);
-}
+// gelu_f / gelu_grad_f / pack_bf16x2 live in common.cuh (shared with the
+// fused GELU + quantize path).
 
 __global__ void gelu_fwd_kernel(const uint4 *__restrict__ H, uint4 *__restrict__ A, int64_t n8) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
@@ -33,7 +21,7 @@ __global__ void gelu_fwd_kernel(const uint4 *__restrict__ H, uint4 *__restrict__
     const uint32_t w[4] = {h.x, h.y, h.z, h.w};
     uint32_t o[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) o[k] = pack_bf16(gelu_f(bf16lo(w[k])), gelu_f(bf16hi(w[k])));
+    for (int k = 0; k < 4; ++k) o[k] = pack_bf16x2(gelu_f(bf16lo(w[k])), gelu_f(bf16hi(w[k])));
     A[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
@@ -47,7 +35,7 @@ __global__ void gelu_bwd_kernel(const uint4 *__restrict__ dA, const uint4 *__res
     uint32_t o[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      o[k] = pack_bf16(__fmul_rn(bf16lo(dw[k]), gelu_grad_f(bf16lo(hw[k]))),
+      o[k] = pack_bf16x2(__fmul_rn(bf16lo(dw[k]), gelu_grad_f(bf16lo(hw[k]))),
                        __fmul_rn(bf16hi(dw[k]), gelu_grad_f(bf16hi(hw[k]))));
     dH[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }

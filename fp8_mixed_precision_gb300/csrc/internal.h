@@ -45,6 +45,13 @@ cudaError_t launch_quantize_delayed(const void *x, int64_t rows, int64_t cols, i
                                     float *scale_inv, float *hist, int hist_len, int64_t step,
                                     float *partials, cudaStream_t st);
 
+// Fused GELU (bwd = 0: A = GELU(H), E4M3) or GELU backward (bwd = 1:
+// dH = H * GELU'(H2) with H = dA, E5M2) with the 1x128 quantizer.
+cudaError_t launch_gelu_quantize(const void *H, const void *H2, int64_t rows, int64_t cols,
+                                 int bwd, uint8_t *out_row, uint8_t *out_col, float *row_scale,
+                                 float *row_scale_inv, float *col_scale, float *col_scale_inv,
+                                 cudaStream_t st);
+
 // FP8 GEMM (tcgen05).  scaling: fp8_scaling.  ws may be null when
 // gemm_workspace_bytes() is 0.
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int scaling);

@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_partials_kernel(const uint4
 // ---------------------------------------------------------------------------
 struct QParams {
   const uint16_t *x;
+  const uint16_t *x2;  // fused GELU backward: H (x holds dA)
   int64_t R, C;
   uint8_t *out_row;  // [R, C] or null
   uint8_t *out_col;  // [C, R] or null
@@ -172,8 +173,15 @@ __device__ __forceinline__ void unpack8(uint4 w, float (&v)[8]) {
   v[4] = bf16lo(w.z); v[5] = bf16hi(w.z); v[6] = bf16lo(w.w); v[7] = bf16hi(w.w);
 }
 
-template <int MODE, int FMT>
+// PRE selects a producer fused in front of the quantizer, applied to the
+// staged tile in shared memory and rounded to bf16 exactly as the standalone
+// kernels round (so fused and unfused results are bitwise equal):
+//   0  none
+//   1  A = bf16(GELU(x))                 (activation of the next linear)
+//   2  dH = bf16(x * GELU'(x2)), x = dA  (gradient entering the linear below)
+template <int MODE, int FMT, int PRE = 0>
 __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
+  static_assert(PRE == 0 || MODE == Q_BLOCK1x128, "fused producers use 1x128 blocks");
   extern __shared__ uint8_t q_smem_raw[];
   QSmem &S = *reinterpret_cast<QSmem *>(q_smem_raw);
 
@@ -183,8 +191,8 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
   const int64_t tiles_r = (p.R + 127) / 128, tiles_c = (p.C + 127) / 128;
   const int64_t ntiles = tiles_r * tiles_c;
 
-  // stage tile `id` into buffer b (zero fill outside the tensor)
-  auto prefetch = [&](int64_t id, int b) {
+  // stage tile `id` of `src` into buffer b (zero fill outside the tensor)
+  auto stage = [&](const uint16_t *srcbase, int64_t id, int b) {
     if (id < ntiles) {
       const int64_t tr = id / tiles_c, tc = id % tiles_c;
       const int64_t r0 = tr * 128, c0 = tc * 128;
@@ -193,10 +201,13 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
       for (int i = 0; i < 8; ++i) {
         const int r = rr + 16 * i;
         const bool ok = col_ok && r0 + r < p.R;
-        const uint16_t *src = ok ? p.x + (r0 + r) * p.C + c0 + 8 * cg : p.x;
+        const uint16_t *src = ok ? srcbase + (r0 + r) * p.C + c0 + 8 * cg : srcbase;
         cp_async16(&S.in[b][r * 128 + 8 * cg], src, ok);
       }
     }
+  };
+  auto prefetch = [&](int64_t id, int b) {
+    if (PRE != 2) stage(p.x, id, b);
     cp_async_commit();
   };
 
@@ -237,15 +248,44 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
   prefetch(id, 0);
   prefetch(id + gridDim.x, 1);
   for (int k = 0; id < ntiles; ++k, id += gridDim.x) {
-    const int b = k & 1;
-    const uint16_t *in = S.in[b];
+    const int b = PRE == 2 ? 0 : (k & 1);
+    uint16_t *in = S.in[b];
     const int64_t tr = id / tiles_c, tc = id % tiles_c;
     const int64_t r0 = tr * 128, c0 = tc * 128;
     const int rows_here = (int)(p.R - r0 < 128 ? p.R - r0 : 128);
     const int cols_here = (int)(p.C - c0 < 128 ? p.C - c0 : 128);
     const bool col_ok = 8 * cg < cols_here;
-    cp_async_wait1();
+    if (PRE == 2) {  // dA and H of this tile into the two buffers (no cross-tile overlap)
+      stage(p.x, id, 0);
+      stage(p.x2, id, 1);
+      cp_async_commit();
+      asm volatile("cp.async.wait_all;" ::: "memory");
+    } else {
+      cp_async_wait1();
+    }
     __syncthreads();  // this tile is in shared memory for every thread
+    if (PRE != 0) {   // fused producer, in place, rounded to bf16
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint4 *pw = reinterpret_cast<uint4 *>(&in[(rr + 16 * i) * 128 + 8 * cg]);
+        const uint4 w = *pw;
+        const uint32_t wi[4] = {w.x, w.y, w.z, w.w};
+        uint32_t o4[4];
+        if (PRE == 1) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) o4[j] = pack_bf16x2(gelu_f(bf16lo(wi[j])), gelu_f(bf16hi(wi[j])));
+        } else {
+          const uint4 hw = *reinterpret_cast<const uint4 *>(&S.in[1][(rr + 16 * i) * 128 + 8 * cg]);
+          const uint32_t hi4[4] = {hw.x, hw.y, hw.z, hw.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            o4[j] = pack_bf16x2(__fmul_rn(bf16lo(wi[j]), gelu_grad_f(bf16lo(hi4[j]))),
+                                __fmul_rn(bf16hi(wi[j]), gelu_grad_f(bf16hi(hi4[j]))));
+        }
+        *pw = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+      }
+      __syncthreads();
+    }
 
     // ---- maxima: one pass over the tile with packed bf16 |max|
     float s_tile = ts;
@@ -454,14 +494,15 @@ int tensorwise_partials_count(int64_t rows, int64_t cols) {
   return (int)std::max<int64_t>(1, std::min<int64_t>(want, cap));
 }
 
-template <int MODE, int FMT>
+template <int MODE, int FMT, int PRE = 0>
 static cudaError_t launch_tile(const QParams &p, cudaStream_t st) {
   static const char *names[3] = {"quant_cast_tensorwise", "quant_block_1x128", "quant_block_128x128"};
+  static const char *pre_names[3] = {"", "gelu_quant_block_1x128", "gelu_bwd_quant_block_1x128"};
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(quant_tile_kernel<MODE, FMT>,
+    cudaError_t e = cudaFuncSetAttribute(quant_tile_kernel<MODE, FMT, PRE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kQSmemBytes);
     if (e != cudaSuccess) return e;
@@ -479,8 +520,9 @@ static cudaError_t launch_tile(const QParams &p, cudaStream_t st) {
     bytes += 16.0 * ntiles;
   else
     bytes += 16.0;
-  LaunchScope ls(names[MODE], st, bytes, 0.0);
-  quant_tile_kernel<MODE, FMT><<<(unsigned)grid, kQThreads, kQSmemBytes, st>>>(p);
+  if (PRE == 2) bytes += 2.0 * p.R * p.C;  // the second input (H)
+  LaunchScope ls(PRE ? pre_names[PRE] : names[MODE], st, bytes, 0.0);
+  quant_tile_kernel<MODE, FMT, PRE><<<(unsigned)grid, kQThreads, kQSmemBytes, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -490,6 +532,7 @@ cudaError_t launch_quantize(const void *x, int64_t rows, int64_t cols, int mode,
                             float *partials, cudaStream_t st) {
   QParams p;
   p.x = static_cast<const uint16_t *>(x);
+  p.x2 = nullptr;
   p.R = rows;
   p.C = cols;
   p.out_row = out_row;
@@ -529,6 +572,7 @@ cudaError_t launch_quantize_delayed(const void *x, int64_t rows, int64_t cols, i
                                     float *partials, cudaStream_t st) {
   QParams p;
   p.x = static_cast<const uint16_t *>(x);
+  p.x2 = nullptr;
   p.R = rows;
   p.C = cols;
   p.out_row = out_row;
@@ -550,6 +594,30 @@ cudaError_t launch_quantize_delayed(const void *x, int64_t rows, int64_t cols, i
   LaunchScope ls("quant_delayed_history", st, 4.0 * grid + 4.0, 0.0);
   delayed_history_update_kernel<<<1, 256, 0, st>>>(partials, grid, hist, hist_len, step);
   return cudaGetLastError();
+}
+
+cudaError_t launch_gelu_quantize(const void *H, const void *H2, int64_t rows, int64_t cols,
+                                 int bwd, uint8_t *out_row, uint8_t *out_col, float *row_scale,
+                                 float *row_scale_inv, float *col_scale, float *col_scale_inv,
+                                 cudaStream_t st) {
+  QParams p;
+  p.x = static_cast<const uint16_t *>(H);
+  p.x2 = static_cast<const uint16_t *>(H2);
+  p.R = rows;
+  p.C = cols;
+  p.out_row = out_row;
+  p.out_col = out_col;
+  p.row_scale = row_scale;
+  p.row_scale_inv = row_scale_inv;
+  p.col_scale = col_scale;
+  p.col_scale_inv = col_scale_inv;
+  p.partials = nullptr;
+  p.n_partials = 0;
+  p.hist = nullptr;
+  p.hist_len = 0;
+  p.cur_partials = nullptr;
+  return bwd ? launch_tile<Q_BLOCK1x128, FP8_FORMAT_E5M2, 2>(p, st)
+             : launch_tile<Q_BLOCK1x128, FP8_FORMAT_E4M3, 1>(p, st);
 }
 
 }  // namespace fp8lin

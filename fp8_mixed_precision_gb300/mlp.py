@@ -18,9 +18,15 @@ from fp8_mixed_precision_gb300 import synthetic as syn
 
 
 class FP8MLPStack:
+    """fused (block recipe only): GELU forward is fused with the quantization
+    of fc2's input and GELU backward with the quantization of fc1's incoming
+    gradient, so the bf16 A and dH tensors are never written; results are
+    bitwise identical to the unfused path."""
+
     def __init__(self, d: int, ffn: int, n_layers: int, n_tokens: int, recipe: str = "block",
-                 device="cuda", seed: int = 43):
+                 device="cuda", seed: int = 43, fused: bool = False):
         self.d, self.ffn, self.L, self.N, self.recipe = d, ffn, n_layers, n_tokens, recipe
+        self.fused = bool(fused) and recipe == "block"
         dev = torch.device(device)
         self.dev = dev
         self.cache = fp.WeightCache()
@@ -44,10 +50,18 @@ class FP8MLPStack:
         self.ctx2 = [fp.LinearContext(fp._empty_bytes(fp._ctx_bytes(recipe, N, ffn), dev), N, ffn)
                      for _ in range(n_layers)]
         self.H = [torch.empty((N, ffn), dtype=torch.bfloat16, device=dev) for _ in range(n_layers)]
-        self.A = [torch.empty((N, ffn), dtype=torch.bfloat16, device=dev) for _ in range(n_layers)]
+        if self.fused:
+            # fc2's quantized input: rowwise in a buffer, transposed inside fc2's context
+            self.Aq = [fp.QuantizedTensor(N, ffn, "act", dev,
+                                          col_ptrs=fp.fp8_linear_ctx_layout(recipe, self.ctx2[l]))
+                       for l in range(n_layers)]
+            self.dHq = fp.QuantizedTensor(N, ffn, "grad", dev)
+            self.A = None
+        else:
+            self.A = [torch.empty((N, ffn), dtype=torch.bfloat16, device=dev) for _ in range(n_layers)]
         self.Y = [torch.empty((N, d), dtype=torch.bfloat16, device=dev) for _ in range(n_layers)]
         self.dA = torch.empty((N, ffn), dtype=torch.bfloat16, device=dev)
-        self.dH = torch.empty((N, ffn), dtype=torch.bfloat16, device=dev)
+        self.dH = None if self.fused else torch.empty((N, ffn), dtype=torch.bfloat16, device=dev)
         self.g = [torch.empty((N, d), dtype=torch.bfloat16, device=dev) for _ in range(2)]
         self.dwb1 = torch.empty((ffn, d), dtype=torch.bfloat16, device=dev)
         self.dwb2 = torch.empty((d, ffn), dtype=torch.bfloat16, device=dev)
@@ -66,19 +80,29 @@ class FP8MLPStack:
         for l in range(self.L):
             self.requantized += c.get(self.h1[l], self.version, use_cache)
             fp.fp8_linear_fwd(h, c, self.h1[l], r, ws=self.ws, y=self.H[l], ctx=self.ctx1[l])
-            fp.fp8_gelu_fwd(self.H[l], out=self.A[l])
             self.requantized += c.get(self.h2[l], self.version, use_cache)
-            fp.fp8_linear_fwd(self.A[l], c, self.h2[l], r, ws=self.ws, y=self.Y[l], ctx=self.ctx2[l])
+            if self.fused:
+                fp.fp8_gelu_quantize(self.H[l], self.Aq[l], r)
+                fp.fp8_linear_fwd_quantized(self.Aq[l], c, self.h2[l], r, self.ws, self.Y[l])
+            else:
+                fp.fp8_gelu_fwd(self.H[l], out=self.A[l])
+                fp.fp8_linear_fwd(self.A[l], c, self.h2[l], r, ws=self.ws, y=self.Y[l],
+                                  ctx=self.ctx2[l])
             h = self.Y[l]
         g = dy
         for l in reversed(range(self.L)):
             fp.fp8_linear_bwd(g, self.ctx2[l], c, self.h2[l], r, ws=self.ws, dx=self.dA,
                               dw=self.dwb2)
             fp.fp8_grad_accumulate(self.dw2[l], self.dwb2)
-            fp.fp8_gelu_bwd(self.dA, self.H[l], out=self.dH)
             out = self.g[l % 2]
-            fp.fp8_linear_bwd(self.dH, self.ctx1[l], c, self.h1[l], r, ws=self.ws, dx=out,
-                              dw=self.dwb1)
+            if self.fused:
+                fp.fp8_gelu_bwd_quantize(self.dA, self.H[l], self.dHq, r)
+                fp.fp8_linear_bwd_quantized(self.dHq, self.ctx1[l], c, self.h1[l], r, self.ws, out,
+                                            self.dwb1)
+            else:
+                fp.fp8_gelu_bwd(self.dA, self.H[l], out=self.dH)
+                fp.fp8_linear_bwd(self.dH, self.ctx1[l], c, self.h1[l], r, ws=self.ws, dx=out,
+                                  dw=self.dwb1)
             fp.fp8_grad_accumulate(self.dw1[l], self.dwb1)
             g = out
         return self.Y[self.L - 1], g

@@ -243,6 +243,45 @@ fp8_status fp8_linear_bwd(const void *dY, int64_t N, int64_t O, const void *ctx,
                           fp8_weight_cache *cache, fp8_weight_handle h, fp8_recipe recipe,
                           void *dX, void *dW, void *ws, size_t ws_bytes, fp8_stream_t stream);
 
+/* ------------------------------------------------------------------ fused producers
+ * Quantization fused into the producer of the quantized tensor (block recipe
+ * only; other recipes return FP8_ERR_UNSUPPORTED).  The bf16 intermediate is
+ * never written: each kernel computes it in fp32, rounds it to bf16 exactly
+ * as fp8_gelu_fwd / fp8_gelu_bwd do, and quantizes that value, so the bytes
+ * and scales equal those of the unfused sequence bit for bit.
+ *   fp8_gelu_quantize:     A = bf16(GELU(H)), 1x128 E4M3 (activation role)
+ *   fp8_gelu_bwd_quantize: dH = bf16(dA * GELU'(H)), 1x128 E5M2 (gradient role)
+ * Output arguments as in fp8_quantize (both layouts optional, not both NULL).
+ * Errors: UNSUPPORTED, INVALID_ARG, SHAPE, ALIGN, CUDA. */
+fp8_status fp8_gelu_quantize(const void *H, int64_t rows, int64_t cols, fp8_recipe recipe,
+                             uint8_t *rowwise_out, uint8_t *colwise_out, float *row_scale,
+                             float *row_scale_inv, float *col_scale, float *col_scale_inv,
+                             fp8_stream_t stream);
+fp8_status fp8_gelu_bwd_quantize(const void *dA, const void *H, int64_t rows, int64_t cols,
+                                 fp8_recipe recipe, uint8_t *rowwise_out, uint8_t *colwise_out,
+                                 float *row_scale, float *row_scale_inv, float *col_scale,
+                                 float *col_scale_inv, fp8_stream_t stream);
+
+/* Linear layer on operands quantized by the caller (e.g. by a fused producer).
+ * fp8_linear_ctx_layout returns where, inside a linear context buffer, the
+ * transposed FP8 input and its scale arrays live, so a producer can write the
+ * saved operand directly.  fp8_linear_fwd_quantized = the fprop GEMM of
+ * fp8_linear_fwd with X given as its rowwise bytes and scale_inv (the caller
+ * has already filled the context's transposed part); fp8_linear_bwd_quantized
+ * = the dgrad (dX may be NULL) and wgrad GEMMs of fp8_linear_bwd with dY
+ * given in both layouts.  Same weight-cache and recipe rules as the bf16 calls. */
+fp8_status fp8_linear_ctx_layout(fp8_recipe recipe, int64_t N, int64_t K, void *ctx,
+                                 uint8_t **xq_col, float **col_scale, float **col_scale_inv);
+fp8_status fp8_linear_fwd_quantized(const uint8_t *xq_row, const float *xq_row_scale_inv,
+                                    int64_t N, int64_t K, fp8_weight_cache *cache,
+                                    fp8_weight_handle h, fp8_recipe recipe, void *Y, void *ws,
+                                    size_t ws_bytes, fp8_stream_t stream);
+fp8_status fp8_linear_bwd_quantized(const uint8_t *gq_row, const float *gq_row_scale_inv,
+                                    const uint8_t *gq_col, const float *gq_col_scale_inv,
+                                    int64_t N, int64_t O, const void *ctx, fp8_weight_cache *cache,
+                                    fp8_weight_handle h, fp8_recipe recipe, void *dX, void *dW,
+                                    void *ws, size_t ws_bytes, fp8_stream_t stream);
+
 /* ------------------------------------------------------------------ MLP glue
  * GELU in its exact erf form, fp32 arithmetic, bf16 in/out, n elements
  * (n a multiple of 8): A = H * Phi(H); dH = dA * (Phi(H) + H * phi(H)).

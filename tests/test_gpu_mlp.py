@@ -179,3 +179,39 @@ def test_large_block_linear_sampled_tiles(fp):
         A = o.dequantize(gc["col"], gc["col_scale_inv"], "e5m2")
         B = o.dequantize(xc["col"], xc["col_scale_inv"], "e4m3")
         check_gemm(dw[sl(tn), sl(tk)], A @ B.T, np.abs(A) @ np.abs(B).T, N, f"dW tile {tn},{tk}")
+
+
+@pytest.mark.parametrize("N", [1024, 400])
+def test_fused_gelu_quantize_equals_unfused(fp, N):
+    """Quantization fused into the GELU producers gives the bytes and scales
+    of the unfused sequence (GELU to bf16, then quantize) bit for bit."""
+    F = 384
+    h = syn.bf16_normal((N, F), 2.0, 81, device="cuda", outlier_frac=0.01)
+    da = syn.bf16_normal((N, F), 1e-3, 82, device="cuda")
+    qf = fp.fp8_gelu_quantize(h, fp.QuantizedTensor(N, F, "act", "cuda"))
+    ref = fp.fp8_quantize(fp.fp8_gelu_fwd(h), "block", "act")
+    gf = fp.fp8_gelu_bwd_quantize(da, h, fp.QuantizedTensor(N, F, "grad", "cuda"))
+    gref = fp.fp8_quantize(fp.fp8_gelu_bwd(da, h), "block", "grad")
+    torch.cuda.synchronize()
+    for got, exp in ((qf, ref), (gf, gref)):
+        assert torch.equal(got.row, exp["row"]) and torch.equal(got.col, exp["col"])
+        for k in ("row_scale", "row_scale_inv", "col_scale", "col_scale_inv"):
+            assert torch.equal(getattr(got, k).view(torch.int32), exp[k].view(torch.int32)), k
+
+
+def test_fused_mlp_stack_equals_unfused(fp):
+    from fp8_mixed_precision_gb300.mlp import FP8MLPStack
+    d, ffn, N, L, GA = 512, 1024, 768, 2, 2
+    xs = [syn.bf16_normal((N, d), 1.0, 900 + i, device="cuda") for i in range(GA)]
+    dys = [syn.bf16_normal((N, d), 1e-3, 910 + i, device="cuda") for i in range(GA)]
+    res = {}
+    for fused in (False, True):
+        st = FP8MLPStack(d, ffn, L, N, "block", fused=fused)
+        outs = st.step(xs, dys, True)
+        torch.cuda.synchronize()
+        res[fused] = (outs, [t.clone() for t in st.dw1 + st.dw2])
+    for (y1, dx1), (y2, dx2) in zip(res[False][0], res[True][0]):
+        assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+        assert torch.equal(dx1.view(torch.int16), dx2.view(torch.int16))
+    for a, b in zip(res[False][1], res[True][1]):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
