@@ -40,30 +40,46 @@ constexpr int BM = 128, BK = 128;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 512;
-// bf16 output staging: per epilogue warp two 32-row x 64-column slabs
-// (32 x 128 bytes, 128-byte swizzled) feeding TMA bulk-tensor stores.
+// bf16 output staging: per epilogue warp Cfg::kOutSlabs 32-row x 64-column
+// slabs (32 x 128 bytes, 128-byte swizzled) feeding TMA bulk-tensor stores.
 constexpr int kOutSlabBytes = 32 * 128;
-constexpr int kOutBytes = kEpiWarps * 2 * kOutSlabBytes;
 constexpr int kSmemBudget = 227 * 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s
-constexpr int kSplitTargetCtas = 152;             // split-K fills about this many CTAs
+constexpr int kSplitTargetCtas = 152;  // wave size the plan assumes (one CTA per SM)
 constexpr int kMaxStages = 8;
 
-template <int BN>
+struct SmemCtl {
+  uint64_t full[kMaxStages], empty[kMaxStages];
+  uint64_t acc_full[4], acc_empty[4];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+  float bscale[kEpiWarps][256];  // 1x128 x 1x128: column scales of 4 K blocks x 64 columns
+};
+static_assert(sizeof(SmemCtl) <= 12288, "control block");
+// barriers and flags only (the column-scale area serves 1x128 x 1x128 alone)
+constexpr int kCtlSmall = (int)((offsetof(SmemCtl, bscale) + 127) / 128 * 128);
+
+// MH = M halves per tile.  MH = 2 gives 256 x BN tiles made of two M = 128
+// MMAs sharing each B stage: for BN = 256, 1.5x fewer operand bytes per flop
+// enter the SM.  The two accumulators fill TMEM, so a tile's epilogue does not
+// overlap the next tile's MMAs: used for deep-K tensor-scaled GEMMs only.
+template <int BN, int MH = 1>
 struct Cfg {
-  static constexpr int kStageA = BM * BK;  // bytes
+  static constexpr int kStageA = MH * BM * BK;  // bytes
   static constexpr int kStageB = BN * BK;
   static constexpr int kStageBytes = kStageA + kStageB;
   static constexpr int kAccBufs = (int)kTmemCols / BN;
-  static constexpr int kCtlBytes = 12288;
-  static constexpr int kStages =
-      (kSmemBudget - 1024 - kOutBytes - kCtlBytes) / kStageBytes < kMaxStages
-          ? (kSmemBudget - 1024 - kOutBytes - kCtlBytes) / kStageBytes
-          : kMaxStages;
+  static constexpr int kCtlBytes = MH == 2 ? kCtlSmall : 12288;
+  static constexpr int kOutSlabs = MH == 2 ? 1 : 2;
+  static constexpr int kOutBytes = kEpiWarps * kOutSlabs * kOutSlabBytes;
+  static constexpr int kRing = kSmemBudget - 1024 - kOutBytes - kCtlBytes;
+  static constexpr int kStages = kRing / kStageBytes < kMaxStages ? kRing / kStageBytes : kMaxStages;
   static constexpr size_t kSmemBytes =
       1024 + (size_t)kStages * kStageBytes + (size_t)kOutBytes + kCtlBytes;
   static_assert(kStages >= 2, "shared memory too small for the operand ring");
+  static_assert(MH == 1 || (MH == 2 && kAccBufs == 2), "two M halves fill TMEM exactly");
 };
 
 __device__ unsigned g_gemm_status;
@@ -80,15 +96,6 @@ struct GemmArgs {
   int vec4;              // scale rows are 16-byte aligned in groups of 4 K blocks
 };
 
-struct SmemCtl {
-  uint64_t full[kMaxStages], empty[kMaxStages];
-  uint64_t acc_full[4], acc_empty[4];
-  uint64_t mma_done;
-  uint32_t tmem_base;
-  int abort;
-  float bscale[kEpiWarps][256];  // 1x128 x 1x128: column scales of 4 K blocks x 64 columns
-};
-static_assert(sizeof(SmemCtl) <= 12288, "control block");
 
 // Bounded wait on phase `parity` of `bar`; false on abort or timeout.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort) {
@@ -185,11 +192,12 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
   return d;
 }
 
-template <int SCALING, bool SPLIT, int BN>
+template <int SCALING, bool SPLIT, int BN, int MH>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const GemmArgs g) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, MH>;
+  static_assert(MH == 1 || SCALING == FP8_SCALING_TENSOR, "M halves: tensor scaling only");
   constexpr int kStages = C::kStages;
   constexpr int NB = C::kAccBufs;
   constexpr int kHalf = BN / 2;           // columns per epilogue warp
@@ -205,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *out_stage = smem + (size_t)kStages * C::kStageBytes;
-  SmemCtl *ctl = reinterpret_cast<SmemCtl *>(out_stage + kOutBytes);
+  SmemCtl *ctl = reinterpret_cast<SmemCtl *>(out_stage + C::kOutBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -250,8 +258,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bar(&ctl->empty[stage], phase ^ 1, abort)) { ok = false; break; }
           uint8_t *sa = smem + (size_t)stage * C::kStageBytes;
-          ptx::mbar_arrive_expect_tx(&ctl->full[stage], C::kStageBytes);
-          ptx::tma_load_2d(sa, &tmA, &ctl->full[stage], kb * BK, tm * BM);
+          // an M half that starts past the last row is not loaded (its
+          // accumulator is never stored)
+          const int64_t row0 = (int64_t)tm * MH * BM;
+          const int halves = (MH == 2 && row0 + BM >= g.M) ? 1 : MH;
+          ptx::mbar_arrive_expect_tx(&ctl->full[stage],
+                                     (uint32_t)(C::kStageBytes - (MH - halves) * BM * BK));
+          for (int mh = 0; mh < halves; ++mh)
+            ptx::tma_load_2d(sa + mh * BM * BK, &tmA, &ctl->full[stage], kb * BK,
+                             (int)(row0 + mh * BM));
           ptx::tma_load_2d(sa + C::kStageA, &tmB, &ctl->full[stage], kb * BK, tn * BN);
           last_phase[stage] = (int)phase;
           if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -275,24 +290,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           // tensor scaling: one accumulator per tile; block scaling: one per K block
           const bool first = SCALING != FP8_SCALING_TENSOR || kb == kb0;
           const bool last = SCALING != FP8_SCALING_TENSOR || kb == kb1 - 1;
-          const uint32_t ab = nacc % NB, aph = (nacc / NB) & 1;
-          if (first) {
-            if (!wait_bar(&ctl->acc_empty[ab], aph ^ 1, abort)) { ok = false; break; }
+          if (first) {  // the accumulator buffer(s) of this tile have been drained
+            for (int mh = 0; ok && mh < MH; ++mh) {
+              const uint32_t n = nacc + mh;
+              if (!wait_bar(&ctl->acc_empty[n % NB], ((n / NB) & 1) ^ 1, abort)) ok = false;
+            }
+            if (!ok) break;
             ptx::tc_fence_after();
           }
           if (!wait_bar(&ctl->full[stage], phase, abort)) { ok = false; break; }
           ptx::tc_fence_after();
-          const uint32_t d = tmem + ab * BN;
           const uint32_t a_addr = ptx::smem_u32(smem + (size_t)stage * C::kStageBytes);
-          const uint64_t adesc = ptx::smem_desc_sw128(a_addr);
           const uint64_t bdesc = ptx::smem_desc_sw128(a_addr + C::kStageA);
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)
-            ptx::mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, g.idesc, (!first || k > 0) ? 1u : 0u);
+#pragma unroll
+            for (int mh = 0; mh < MH; ++mh) {
+              const uint32_t d = tmem + ((nacc + mh) % NB) * BN;
+              const uint64_t adesc = ptx::smem_desc_sw128(a_addr + mh * BM * BK);
+              ptx::mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, g.idesc,
+                              (!first || k > 0) ? 1u : 0u);
+            }
           ptx::mma_commit(&ctl->empty[stage]);
           if (last) {
-            ptx::mma_commit(&ctl->acc_full[ab]);
-            ++nacc;
+            for (int mh = 0; mh < MH; ++mh) ptx::mma_commit(&ctl->acc_full[(nacc + mh) % NB]);
+            nacc += MH;
           }
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
@@ -309,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * kHalf);
     uint32_t nacc = 0;
     uint32_t nout = 0;  // bf16 slabs this warp has handed to TMA stores
-    uint8_t *slabs = out_stage + (size_t)(warp - 2) * 2 * kOutSlabBytes;
+    uint8_t *slabs = out_stage + (size_t)(warp - 2) * C::kOutSlabs * kOutSlabBytes;
     float s_tensor = 0.0f;
     if (SCALING == FP8_SCALING_TENSOR) s_tensor = __fmul_rn(g.a_sinv[0], g.b_sinv[0]);
 
@@ -323,8 +345,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
       }
       if (slab_y >= g.M || col0 >= g.N) return;  // slab entirely outside C
-      uint8_t *slab = slabs + (nout & 1) * kOutSlabBytes;
-      if (lane == 0) ptx::bulk_wait_read<1>();  // the store two slabs ago has read this buffer
+      uint8_t *slab = slabs + (nout % C::kOutSlabs) * kOutSlabBytes;
+      // the store kOutSlabs slabs ago has finished reading this buffer
+      if (lane == 0) ptx::bulk_wait_read<C::kOutSlabs - 1>();
       __syncwarp();
       stage32(slab, lane, 0, v0, scale);
       stage32(slab, lane, 4, v1, scale);
@@ -341,34 +364,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       int tm, tn, kb0, kb1;
       decode_unit(g, u, tm, tn, kb0, kb1);
       const int split = (int)(u % g.splits);
-      const int64_t m = (int64_t)tm * BM + r;
+      const int64_t m = (int64_t)tm * MH * BM + r;
       const int64_t colbase = (int64_t)tn * BN + h * kHalf;
-      const int64_t slab_y = (int64_t)tm * BM + q * 32;
+      const int64_t slab_y0 = (int64_t)tm * MH * BM + q * 32;
       if (SCALING == FP8_SCALING_TENSOR) {
-        const uint32_t ab = nacc % NB, aph = (nacc / NB) & 1;
-        if (!wait_bar(&ctl->acc_full[ab], aph, abort)) break;
-        ptx::tc_fence_after();
+        bool ok = true;
+        for (int mh = 0; mh < MH; ++mh) {  // one accumulator buffer per M half
+          const int64_t slab_y = slab_y0 + (int64_t)mh * BM;
+          const uint32_t ab = nacc % NB, aph = (nacc / NB) & 1;
+          if (!wait_bar(&ctl->acc_full[ab], aph, abort)) { ok = false; break; }
+          ptx::tc_fence_after();
 #pragma unroll
-        for (int s = 0; s < kSlabs; ++s) {
-          uint32_t raw0[32], raw1[32];
-          ptx::tmem_ld32(tl + ab * BN + 64 * s, raw0);
-          ptx::tmem_ld32(tl + ab * BN + 64 * s + 32, raw1);
-          ptx::tmem_ld_wait();
-          if (s == kSlabs - 1) {  // accumulator fully in registers: free the TMEM buffer
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty[ab]);
-          }
-          float v0[32], v1[32];
+          for (int s = 0; s < kSlabs; ++s) {
+            uint32_t raw0[32], raw1[32];
+            ptx::tmem_ld32(tl + ab * BN + 64 * s, raw0);
+            ptx::tmem_ld32(tl + ab * BN + 64 * s + 32, raw1);
+            ptx::tmem_ld_wait();
+            if (s == kSlabs - 1) {  // accumulator fully in registers: free the TMEM buffer
+              ptx::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty[ab]);
+            }
+            float v0[32], v1[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            v0[j] = __uint_as_float(raw0[j]);
-            v1[j] = __uint_as_float(raw1[j]);
+            for (int j = 0; j < 32; ++j) {
+              v0[j] = __uint_as_float(raw0[j]);
+              v1[j] = __uint_as_float(raw1[j]);
+            }
+            emit(v0, v1, s_tensor, colbase + 64 * s, slab_y, split);
           }
-          emit(v0, v1, s_tensor, colbase + 64 * s, slab_y, split);
+          ++nacc;
         }
-        ++nacc;
+        if (!ok) break;
       } else {
+        const int64_t slab_y = slab_y0;
         uint64_t acc[kHalf / 2];  // kHalf fp32 accumulators as packed pairs
 #pragma unroll
         for (int j = 0; j < kHalf / 2; ++j) acc[j] = 0;
@@ -603,41 +632,77 @@ bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int 
 }
 
 struct Plan {
-  int bn, tiles_m, tiles_n, kbs, splits, kb_per_split;
+  int bn, mh, tiles_m, tiles_n, kbs, splits, kb_per_split;
+  double est_s;  // estimated kernel time, seconds (plan selection only)
 };
 
-// Kernel configuration as a function of (M, N, K, scaling) only.
-Plan make_plan(int64_t M, int64_t N, int64_t K, int scaling) {
+// Per-SM operand rates used to compare plans (seconds per 128-deep K block of
+// one tile): a 128 x 256 tile is limited by the operand bytes entering the
+// SM (~17 TFLOP/s per SM); a 256 x 256 tile moves 1.5x fewer bytes per flop.
+constexpr double kSmFlopsBn256Mh1 = 17e12, kSmFlopsBn256Mh2 = 22e12, kSmFlopsBn128 = 14e12;
+constexpr double kPlanHbmBps = 6e12;        // fp32 split partials, written and read once
+constexpr double kPlanEpiBps = 30e9;        // per-SM epilogue drain rate (not overlapped, MH = 2)
+constexpr double kPlanReduceLaunchS = 4e-6;
+
+// One candidate: tile shape (bn, mh) and the split count that minimises
+// waves x (K blocks per unit x time per K block [+ unoverlapped epilogue])
+// + split-partial traffic.  Splits start on 4-block groups.
+Plan plan_for(int64_t M, int64_t N, int64_t K, int bn, int mh) {
   Plan p;
-  // 256-wide tiles halve the A re-reads and the per-SM operand traffic per
-  // flop; the 1x128 x 1x128 promotion needs per-column scales and stays 128-wide
-  p.bn = (N >= 256 && scaling != FP8_SCALING_1x128_1x128) ? 256 : 128;
-  p.tiles_m = (int)((M + BM - 1) / BM);
-  p.tiles_n = (int)((N + p.bn - 1) / p.bn);
+  p.bn = bn;
+  p.mh = mh;
+  p.tiles_m = (int)((M + BM * mh - 1) / (BM * mh));
+  p.tiles_n = (int)((N + bn - 1) / bn);
   p.kbs = (int)((K + BK - 1) / BK);
   const int64_t tiles = (int64_t)p.tiles_m * p.tiles_n;
-  int s = 1;
-  if (tiles < kSplitTargetCtas) {
-    s = (int)(kSplitTargetCtas / tiles);
-    s = std::min(s, std::max(1, p.kbs / 4));  // at least 4 K blocks per split
-    s = std::min(s, 32);
-    s = std::max(s, 1);
+  const double rate = bn == 128 ? kSmFlopsBn128 : (mh == 2 ? kSmFlopsBn256Mh2 : kSmFlopsBn256Mh1);
+  const double t_kb = 2.0 * BM * mh * bn * BK / rate;
+  p.splits = 1;
+  p.kb_per_split = p.kbs;
+  p.est_s = 1e30;
+  const int max_s = std::min(32, std::max(1, p.kbs / 4));
+  for (int s = 1; s <= max_s; ++s) {
+    int kbp = (p.kbs + s - 1) / s;
+    if (s > 1) kbp = (kbp + 3) / 4 * 4;
+    const int splits = (p.kbs + kbp - 1) / kbp;
+    if (splits != s) continue;  // same as a smaller split count
+    const int64_t units = tiles * splits;
+    const int64_t waves = (units + kSplitTargetCtas - 1) / kSplitTargetCtas;
+    double unit_s = kbp * t_kb;
+    if (mh == 2) unit_s += (double)BM * mh * bn * (splits > 1 ? 4 : 2) / kPlanEpiBps;
+    double est = (double)waves * unit_s;
+    if (splits > 1) est += 8.0 * splits * M * N / kPlanHbmBps + kPlanReduceLaunchS;
+    if (est < p.est_s * 0.98) {  // a larger split must win clearly
+      p.est_s = est;
+      p.splits = splits;
+      p.kb_per_split = kbp;
+    }
   }
-  p.kb_per_split = (p.kbs + s - 1) / s;
-  if (s > 1) p.kb_per_split = (p.kb_per_split + 3) / 4 * 4;  // splits start on 4-block groups
-  p.splits = (p.kbs + p.kb_per_split - 1) / p.kb_per_split;
   return p;
 }
 
-template <int SCALING, bool SPLIT, int BN>
+// Kernel configuration as a function of (M, N, K, scaling) only.
+Plan make_plan(int64_t M, int64_t N, int64_t K, int scaling) {
+  // 256-wide tiles halve the A re-reads and the per-SM operand traffic per
+  // flop; the 1x128 x 1x128 promotion needs per-column scales and stays 128-wide
+  const int bn = (N >= 256 && scaling != FP8_SCALING_1x128_1x128) ? 256 : 128;
+  Plan p = plan_for(M, N, K, bn, 1);
+  if (scaling == FP8_SCALING_TENSOR && bn == 256 && M > BM) {
+    const Plan p2 = plan_for(M, N, K, bn, 2);
+    if (p2.est_s < p.est_s) p = p2;
+  }
+  return p;
+}
+
+template <int SCALING, bool SPLIT, int BN, int MH = 1>
 cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
                            const GemmArgs &g, cudaStream_t st) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, MH>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(fp8_gemm_kernel<SCALING, SPLIT, BN>,
+    cudaError_t e = cudaFuncSetAttribute(fp8_gemm_kernel<SCALING, SPLIT, BN, MH>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -651,14 +716,19 @@ cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const C
   if (SCALING == FP8_SCALING_1x128_128x128) bytes += 4.0 * g.kbs * (g.M + (g.N + 127) / 128);
   if (SCALING == FP8_SCALING_1x128_1x128) bytes += 4.0 * g.kbs * (g.M + g.N);
   LaunchScope ls(names[SCALING], st, bytes, 2.0 * g.M * g.N * g.K);
-  fp8_gemm_kernel<SCALING, SPLIT, BN><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(ta, tb, tc,
-                                                                                       g);
+  fp8_gemm_kernel<SCALING, SPLIT, BN, MH>
+      <<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(ta, tb, tc, g);
   return cudaGetLastError();
 }
 
 template <int SCALING>
 cudaError_t launch_scaling(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
-                           const GemmArgs &g, bool split, int bn, cudaStream_t st) {
+                           const GemmArgs &g, bool split, int bn, int mh, cudaStream_t st) {
+  if constexpr (SCALING == FP8_SCALING_TENSOR) {
+    if (bn == 256 && mh == 2)
+      return split ? launch_variant<SCALING, true, 256, 2>(ta, tb, tc, g, st)
+                   : launch_variant<SCALING, false, 256, 2>(ta, tb, tc, g, st);
+  }
   if constexpr (SCALING != FP8_SCALING_1x128_1x128) {
     if (bn == 256)
       return split ? launch_variant<SCALING, true, 256>(ta, tb, tc, g, st)
@@ -711,13 +781,13 @@ cudaError_t launch_gemm(const uint8_t *A, int a_fmt, const float *a_sinv, const 
   cudaError_t e;
   switch (scaling) {
     case FP8_SCALING_TENSOR:
-      e = launch_scaling<FP8_SCALING_TENSOR>(ta, tb, tc, g, split, p.bn, st);
+      e = launch_scaling<FP8_SCALING_TENSOR>(ta, tb, tc, g, split, p.bn, p.mh, st);
       break;
     case FP8_SCALING_1x128_128x128:
-      e = launch_scaling<FP8_SCALING_1x128_128x128>(ta, tb, tc, g, split, p.bn, st);
+      e = launch_scaling<FP8_SCALING_1x128_128x128>(ta, tb, tc, g, split, p.bn, p.mh, st);
       break;
     default:
-      e = launch_scaling<FP8_SCALING_1x128_1x128>(ta, tb, tc, g, split, p.bn, st);
+      e = launch_scaling<FP8_SCALING_1x128_1x128>(ta, tb, tc, g, split, p.bn, p.mh, st);
       break;
   }
   if (e != cudaSuccess || !split) return e;

@@ -61,6 +61,21 @@ def test_gemm_parity(fp, M, N, K, scaling):
     _run(fp, M, N, K, scaling)
 
 
+@pytest.mark.parametrize("M,N,K", [(8192, 512, 512), (8320, 400, 496), (16384, 2048, 256)])
+def test_gemm_short_k_many_tiles(fp, M, N, K):
+    # output-bound shapes: many M tiles over a short (ragged) K
+    _run(fp, M, N, K, "tensor", "e4m3", "e4m3", seed=M + N)
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 2048, 4096), (8400, 768, 4096), (8320, 768, 4096),
+                                   (4096, 768, 16384)])
+def test_gemm_deep_k_tensor(fp, M, N, K):
+    # deep-K tensor-scaled shapes (256-row tiles of two M halves); ragged last
+    # tiles with a partial second half (8400) and a second half past M (8320);
+    # split-K over such tiles (K = 16384)
+    _run(fp, M, N, K, "tensor", "e4m3", "e5m2", seed=K + M)
+
+
 @pytest.mark.parametrize("afmt,bfmt", [("e4m3", "e4m3"), ("e5m2", "e4m3"), ("e4m3", "e5m2"),
                                        ("e5m2", "e5m2")])
 def test_gemm_formats(fp, afmt, bfmt):
