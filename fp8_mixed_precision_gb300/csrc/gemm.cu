@@ -28,6 +28,8 @@
 // partial to the workspace; a second kernel sums the splits in a fixed
 // order.  Every wait is bounded: on expiry the kernel records
 // FP8_ERR_TIMEOUT, drains what it has in flight, frees its TMEM and returns.
+#include <cstddef>
+
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -65,14 +67,17 @@ constexpr int kCtlSmall = (int)((offsetof(SmemCtl, bscale) + 127) / 128 * 128);
 // MMAs sharing each B stage: for BN = 256, 1.5x fewer operand bytes per flop
 // enter the SM.  The two accumulators fill TMEM, so a tile's epilogue does not
 // overlap the next tile's MMAs: used for deep-K tensor-scaled GEMMs only.
-template <int BN, int MH = 1>
+// Shared memory: operand ring, bf16 output staging (none for split-K, which
+// writes fp32 partials from registers) and the control block (the column
+// scale area only for 1x128 x 1x128).
+template <int SCALING, bool SPLIT, int BN, int MH = 1>
 struct Cfg {
   static constexpr int kStageA = MH * BM * BK;  // bytes
   static constexpr int kStageB = BN * BK;
   static constexpr int kStageBytes = kStageA + kStageB;
   static constexpr int kAccBufs = (int)kTmemCols / BN;
-  static constexpr int kCtlBytes = MH == 2 ? kCtlSmall : 12288;
-  static constexpr int kOutSlabs = MH == 2 ? 1 : 2;
+  static constexpr int kCtlBytes = SCALING == FP8_SCALING_1x128_1x128 ? 12288 : kCtlSmall;
+  static constexpr int kOutSlabs = SPLIT ? 0 : (MH == 2 ? 1 : 2);
   static constexpr int kOutBytes = kEpiWarps * kOutSlabs * kOutSlabBytes;
   static constexpr int kRing = kSmemBudget - 1024 - kOutBytes - kCtlBytes;
   static constexpr int kStages = kRing / kStageBytes < kMaxStages ? kRing / kStageBytes : kMaxStages;
@@ -196,7 +201,7 @@ template <int SCALING, bool SPLIT, int BN, int MH>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const GemmArgs g) {
-  using C = Cfg<BN, MH>;
+  using C = Cfg<SCALING, SPLIT, BN, MH>;
   static_assert(MH == 1 || SCALING == FP8_SCALING_TENSOR, "M halves: tensor scaling only");
   constexpr int kStages = C::kStages;
   constexpr int NB = C::kAccBufs;
@@ -339,25 +344,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (bf16) or writes it as an fp32 split-K partial.
     auto emit = [&](const float (&v0)[32], const float (&v1)[32], float scale, int64_t col0,
                     int64_t slab_y, int split) {
-      if (SPLIT) {
+      if constexpr (SPLIT) {
         store32_f32(g, split, slab_y + lane, col0, v0, scale);
         store32_f32(g, split, slab_y + lane, col0 + 32, v1, scale);
-        return;
+      } else {
+        if (slab_y >= g.M || col0 >= g.N) return;  // slab entirely outside C
+        uint8_t *slab = slabs + (nout % C::kOutSlabs) * kOutSlabBytes;
+        // the store kOutSlabs slabs ago has finished reading this buffer
+        if (lane == 0) ptx::bulk_wait_read<C::kOutSlabs - 1>();
+        __syncwarp();
+        stage32(slab, lane, 0, v0, scale);
+        stage32(slab, lane, 4, v1, scale);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_2d(&tmC, slab, (int)col0, (int)slab_y);
+          ptx::bulk_commit();
+        }
+        ++nout;
       }
-      if (slab_y >= g.M || col0 >= g.N) return;  // slab entirely outside C
-      uint8_t *slab = slabs + (nout % C::kOutSlabs) * kOutSlabBytes;
-      // the store kOutSlabs slabs ago has finished reading this buffer
-      if (lane == 0) ptx::bulk_wait_read<C::kOutSlabs - 1>();
-      __syncwarp();
-      stage32(slab, lane, 0, v0, scale);
-      stage32(slab, lane, 4, v1, scale);
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        ptx::tma_store_2d(&tmC, slab, (int)col0, (int)slab_y);
-        ptx::bulk_commit();
-      }
-      ++nout;
     };
 
     for (int64_t u = blockIdx.x; u < g.units; u += gridDim.x) {
@@ -636,17 +641,24 @@ struct Plan {
   double est_s;  // estimated kernel time, seconds (plan selection only)
 };
 
-// Per-SM operand rates used to compare plans (seconds per 128-deep K block of
-// one tile): a 128 x 256 tile is limited by the operand bytes entering the
-// SM (~17 TFLOP/s per SM); a 256 x 256 tile moves 1.5x fewer bytes per flop.
-constexpr double kSmFlopsBn256Mh1 = 17e12, kSmFlopsBn256Mh2 = 22e12, kSmFlopsBn128 = 14e12;
-constexpr double kPlanHbmBps = 6e12;        // fp32 split partials, written and read once
-constexpr double kPlanEpiBps = 30e9;        // per-SM epilogue drain rate (not overlapped, MH = 2)
+// Rates used to compare plans (flop/s).  A CTA alone on the GPU runs a
+// 128 x 256 tile at about kSmRate; with every SM busy the operand traffic
+// through L2 caps the whole GPU at about kGpuRate.  A 256 x 256 tile (two M
+// halves) moves 1.5x fewer operand bytes per flop, so both rates are higher.
+struct TileRates {
+  double sm, gpu;
+};
+constexpr TileRates kRatesBn128{14e12, 2.0e15}, kRatesBn256{20e12, 2.6e15},
+    kRatesBn256Mh2{23.5e12, 3.1e15};
+constexpr double kPlanHbmBps = 6e12;   // fp32 split partials, written and read once
+constexpr double kPlanEpiBps = 60e9;   // per-SM epilogue drain rate (not overlapped, MH = 2)
 constexpr double kPlanReduceLaunchS = 4e-6;
 
 // One candidate: tile shape (bn, mh) and the split count that minimises
-// waves x (K blocks per unit x time per K block [+ unoverlapped epilogue])
-// + split-partial traffic.  Splits start on 4-block groups.
+//   max(waves x time per unit, all units' work at the GPU-wide rate)
+//   + split-partial traffic,
+// a unit's time being its K blocks at the per-SM rate plus, for MH = 2, its
+// unoverlapped epilogue.  Splits start on 4-block groups.
 Plan plan_for(int64_t M, int64_t N, int64_t K, int bn, int mh) {
   Plan p;
   p.bn = bn;
@@ -655,8 +667,9 @@ Plan plan_for(int64_t M, int64_t N, int64_t K, int bn, int mh) {
   p.tiles_n = (int)((N + bn - 1) / bn);
   p.kbs = (int)((K + BK - 1) / BK);
   const int64_t tiles = (int64_t)p.tiles_m * p.tiles_n;
-  const double rate = bn == 128 ? kSmFlopsBn128 : (mh == 2 ? kSmFlopsBn256Mh2 : kSmFlopsBn256Mh1);
-  const double t_kb = 2.0 * BM * mh * bn * BK / rate;
+  const TileRates r = bn == 128 ? kRatesBn128 : (mh == 2 ? kRatesBn256Mh2 : kRatesBn256);
+  const double kb_flops = 2.0 * BM * mh * bn * BK;
+  const double all_s = (double)tiles * p.kbs * kb_flops / r.gpu;
   p.splits = 1;
   p.kb_per_split = p.kbs;
   p.est_s = 1e30;
@@ -666,11 +679,10 @@ Plan plan_for(int64_t M, int64_t N, int64_t K, int bn, int mh) {
     if (s > 1) kbp = (kbp + 3) / 4 * 4;
     const int splits = (p.kbs + kbp - 1) / kbp;
     if (splits != s) continue;  // same as a smaller split count
-    const int64_t units = tiles * splits;
-    const int64_t waves = (units + kSplitTargetCtas - 1) / kSplitTargetCtas;
-    double unit_s = kbp * t_kb;
+    const int64_t waves = (tiles * splits + kSplitTargetCtas - 1) / kSplitTargetCtas;
+    double unit_s = kbp * kb_flops / r.sm;
     if (mh == 2) unit_s += (double)BM * mh * bn * (splits > 1 ? 4 : 2) / kPlanEpiBps;
-    double est = (double)waves * unit_s;
+    double est = std::max((double)waves * unit_s, all_s);
     if (splits > 1) est += 8.0 * splits * M * N / kPlanHbmBps + kPlanReduceLaunchS;
     if (est < p.est_s * 0.98) {  // a larger split must win clearly
       p.est_s = est;
@@ -697,7 +709,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int scaling) {
 template <int SCALING, bool SPLIT, int BN, int MH = 1>
 cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
                            const GemmArgs &g, cudaStream_t st) {
-  using C = Cfg<BN, MH>;
+  using C = Cfg<SCALING, SPLIT, BN, MH>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);

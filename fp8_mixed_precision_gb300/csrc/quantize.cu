@@ -43,7 +43,8 @@ constexpr int kAmaxThreads = 512;
 __device__ __forceinline__ int swz(int r) { return ((r >> 4) & 7) << 2; }
 
 // ---------------------------------------------------------------------------
-// Tensorwise pass 1: per-CTA max |x| over a grid-stride sweep (NaN ignored).
+// Tensorwise pass 1: per-CTA max |x| over a grid-stride sweep, first to last
+// (NaN ignored).
 // bf16 magnitudes order like unsigned integers, so the sweep works on the
 // packed bit patterns with SIMD 16-bit max.
 // ---------------------------------------------------------------------------
@@ -82,7 +83,10 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_partials_kernel(const uint4
 }
 
 // ---------------------------------------------------------------------------
-// Fused cast, one 128x128 tile per loop iteration (persistent grid).
+// Fused cast, one 128x128 tile per loop iteration (persistent grid).  Tiles
+// are visited last to first: the amax pass sweeps the tensor first to last,
+// so the cast starts on the rows still in L2, and it finishes on the first
+// rows, which the GEMM that consumes its output reads first.
 // ---------------------------------------------------------------------------
 struct QParams {
   const uint16_t *x;
@@ -194,7 +198,7 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
   // stage tile `id` of `src` into buffer b (zero fill outside the tensor)
   auto stage = [&](const uint16_t *srcbase, int64_t id, int b) {
     if (id < ntiles) {
-      const int64_t tr = id / tiles_c, tc = id % tiles_c;
+      const int64_t tr = (ntiles - 1 - id) / tiles_c, tc = (ntiles - 1 - id) % tiles_c;
       const int64_t r0 = tr * 128, c0 = tc * 128;
       const bool col_ok = c0 + 8 * cg < p.C;
 #pragma unroll
@@ -250,7 +254,7 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
   for (int k = 0; id < ntiles; ++k, id += gridDim.x) {
     const int b = PRE == 2 ? 0 : (k & 1);
     uint16_t *in = S.in[b];
-    const int64_t tr = id / tiles_c, tc = id % tiles_c;
+    const int64_t tr = (ntiles - 1 - id) / tiles_c, tc = (ntiles - 1 - id) % tiles_c;
     const int64_t r0 = tr * 128, c0 = tc * 128;
     const int rows_here = (int)(p.R - r0 < 128 ? p.R - r0 : 128);
     const int cols_here = (int)(p.C - c0 < 128 ? p.C - c0 : 128);
