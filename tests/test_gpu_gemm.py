@@ -76,11 +76,13 @@ def test_gemm_deep_k_tensor(fp, M, N, K):
     _run(fp, M, N, K, "tensor", "e4m3", "e5m2", seed=K + M)
 
 
-@pytest.mark.parametrize("M,N,K", [(4224, 304, 1024), (384, 256, 640), (4224, 304, 32768)])
+@pytest.mark.parametrize("M,N,K", [(4224, 304, 1024), (384, 256, 640), (4224, 304, 32768),
+                                   (3072, 2048, 8192), (4224, 2048, 8192)])
 def test_gemm_tensor_ragged_tiles(fp, M, N, K):
     # an odd number of M tiles, and N = 304: the last 256-wide N tile holds
-    # 48 valid columns, its second 128-column half none; the deep-K case
-    # splits K over 256-row tiles
+    # 48 valid columns, its second 128-column half none.  The K >= 8192
+    # cases run 256-row tiles as CTA pairs (cta_group::2), split over K
+    # (32768) or not (8192), with the last pair's second tile past M (4224)
     _run(fp, M, N, K, "tensor", "e5m2", "e4m3", seed=N + K)
 
 
