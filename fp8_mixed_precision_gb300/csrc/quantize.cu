@@ -291,6 +291,12 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
       __syncthreads();
     }
 
+    // this thread's 8 rows x 8 columns of the tile, read from shared memory
+    // once and kept in registers for the maxima and the cast
+    uint4 xw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) xw[i] = *reinterpret_cast<const uint4 *>(&in[(rr + 16 * i) * 128 + 8 * cg]);
+
     // ---- maxima: one pass over the tile with packed bf16 |max|
     float s_tile = ts;
     uint32_t cm[4] = {0, 0, 0, 0};  // column maxima of this thread's 8 columns (pairs)
@@ -299,7 +305,7 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int r = rr + 16 * i;
-        const uint4 w = *reinterpret_cast<const uint4 *>(&in[r * 128 + 8 * cg]);
+        const uint4 w = xw[i];
         if (MODE == Q_BLOCK1x128) {
           cm[0] = absmax2(cm[0], w.x); cm[1] = absmax2(cm[1], w.y);
           cm[2] = absmax2(cm[2], w.z); cm[3] = absmax2(cm[3], w.w);
@@ -384,7 +390,7 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int r = rr + 16 * i;
-      const uint4 w = *reinterpret_cast<const uint4 *>(&in[r * 128 + 8 * cg]);
+      const uint4 w = xw[i];
       float v[8];
       unpack8(w, v);
       const bool special = nonfinite4(w);
