@@ -144,10 +144,19 @@ __device__ __forceinline__ uint2 cast8(const float (&v)[8], bool special) {
   return q;
 }
 
-__device__ __forceinline__ bool nonfinite4(uint4 w) {
-  const uint32_t e = 0x7F807F80u;
-  return (__vcmpeq2(w.x & e, e) | __vcmpeq2(w.y & e, e) | __vcmpeq2(w.z & e, e) |
-          __vcmpeq2(w.w & e, e)) != 0;
+// True if any of the 64 bf16 values is inf or NaN: a NaN-propagating packed
+// max of the magnitudes reaches the all-ones exponent exactly then.
+__device__ __forceinline__ bool any_nonfinite64(const uint4 (&w)[8]) {
+  __nv_bfloat162 m = __float2bfloat162_rn(0.0f);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t q[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      m = __hmax2_nan(m, __habs2(*reinterpret_cast<const __nv_bfloat162 *>(&q[j])));
+  }
+  const uint32_t b = *reinterpret_cast<uint32_t *>(&m);
+  return (b & 0x7F80u) == 0x7F80u || (b & 0x7F800000u) == 0x7F800000u;
 }
 
 // max(acc, |w|) on packed bf16 pairs; NaN lanes of w are ignored (max.bf16x2
@@ -296,6 +305,8 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
     uint4 xw[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) xw[i] = *reinterpret_cast<const uint4 *>(&in[(rr + 16 * i) * 128 + 8 * cg]);
+    // any inf or NaN among these 64 values selects the cast's NaN fix-up
+    const bool special = any_nonfinite64(xw);
 
     // ---- maxima: one pass over the tile with packed bf16 |max|
     float s_tile = ts;
@@ -393,7 +404,6 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
       const uint4 w = xw[i];
       float v[8];
       unpack8(w, v);
-      const bool special = nonfinite4(w);
       if (MODE == Q_TENSOR && p.cur_partials)
         cur_max = absmax2(absmax2(absmax2(absmax2(cur_max, w.x), w.y), w.z), w.w);
       const float s = MODE == Q_BLOCK1x128 ? S.rowsc[r] : s_tile;
