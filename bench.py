@@ -556,84 +556,90 @@ def run_plain_and_assay(fp, dev, stream):
     return out
 
 
+def _link_GBps(dev, nbytes=1 << 30):
+    """Host<->device link bandwidth with both directions busy at once (pinned
+    buffers, one copy each way), the bound of a copy-limited end-to-end run."""
+    import torch
+    h1 = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h2 = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d1 = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d2 = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    best = 0.0
+    for _ in range(3):
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        s1.wait_stream(torch.cuda.current_stream())
+        s2.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s1):
+            d1.copy_(h1, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h2.copy_(d2, non_blocking=True)
+        torch.cuda.current_stream().wait_stream(s1)
+        torch.cuda.current_stream().wait_stream(s2)
+        b.record()
+        torch.cuda.synchronize()
+        best = max(best, 2 * nbytes / (a.elapsed_time(b) / 1e3) / 1e9)
+    del h1, h2, d1, d2
+    return best
+
+
 def run_e2e(fp, layers, cache, ws, ctx, N, dev, world, args, stream):
-    """Same step through the C ABI with every input copied from pinned host
-    memory and every result copied back inside the timed region.  Copies and
-    compute run on three streams: the host-to-device copies of linear i+1 and
-    the device-to-host copies of linear i-1 overlap the kernels of linear i
-    (per-linear device buffers; cross-step waits keep a buffer from being
-    overwritten while a previous step still reads it)."""
+    """Same step through the C ABI's host-buffer entry point
+    (fp8_linear_step_host): every input is copied from pinned host memory and
+    every result copied back by the library, inside the timed region.  One
+    pipeline slot per linear: the library's copy-in / compute / copy-out
+    streams let the copies of one linear overlap the kernels of another."""
     import torch
     host = []
     h2d = d2h = 0
     for L in layers:
-        hx = torch.empty(L["x"].shape, dtype=torch.bfloat16, pin_memory=True)
-        hw = torch.empty(L["w"].shape, dtype=torch.bfloat16, pin_memory=True)
-        hdy = torch.empty(L["dy"].shape, dtype=torch.bfloat16, pin_memory=True)
-        hx.copy_(L["x"]); hw.copy_(L["w"]); hdy.copy_(L["dy"])
-        hy = torch.empty(L["y"].shape, dtype=torch.bfloat16, pin_memory=True)
-        hdx = torch.empty(L["dx"].shape, dtype=torch.bfloat16, pin_memory=True)
-        hdw = torch.empty(L["dw"].shape, dtype=torch.bfloat16, pin_memory=True)
-        host.append((hx, hw, hdy, hy, hdx, hdw))
-        h2d += 2 * (hx.numel() + hw.numel() + hdy.numel())
-        d2h += 2 * (hy.numel() + hdx.numel() + hdw.numel())
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    n = len(layers)
-    ev_in = [torch.cuda.Event() for _ in range(n)]     # inputs of linear i on the device
-    ev_done = [torch.cuda.Event() for _ in range(n)]   # kernels of linear i finished
-    ev_out = [torch.cuda.Event() for _ in range(n)]    # results of linear i on the host
-    for e in ev_done + ev_out:
-        e.record(stream)
+        hb = {"X": torch.empty(L["x"].shape, dtype=torch.bfloat16, pin_memory=True),
+              "W": torch.empty(L["w"].shape, dtype=torch.bfloat16, pin_memory=True),
+              "dY": torch.empty(L["dy"].shape, dtype=torch.bfloat16, pin_memory=True),
+              "Y": torch.empty(L["y"].shape, dtype=torch.bfloat16, pin_memory=True),
+              "dX": torch.empty(L["dx"].shape, dtype=torch.bfloat16, pin_memory=True),
+              "dW": torch.empty(L["dw"].shape, dtype=torch.bfloat16, pin_memory=True)}
+        hb["X"].copy_(L["x"]); hb["W"].copy_(L["w"]); hb["dY"].copy_(L["dy"])
+        host.append(hb)
+        h2d += 2 * (hb["X"].numel() + hb["W"].numel() + hb["dY"].numel())
+        d2h += 2 * (hb["Y"].numel() + hb["dX"].numel() + hb["dW"].numel())
+    devs = [{"X": L["x"], "dY": L["dy"], "Y": L["y"], "dX": L["dx"], "dW": L["dw"]}
+            for L in layers]
+    pipe = fp.HostPipeline(len(layers))
     version = [10 ** 6]
 
     def step():
         cache.begin_cycle()
         version[0] += 1
-        for i, (L, (hx, hw, hdy, hy, hdx, hdw)) in enumerate(zip(layers, host)):
-            s_in.wait_event(ev_done[i])          # previous step's kernels no longer read them
-            with torch.cuda.stream(s_in):
-                L["x"].copy_(hx, non_blocking=True)
-                L["w"].copy_(hw, non_blocking=True)
-                L["dy"].copy_(hdy, non_blocking=True)
-                ev_in[i].record(s_in)
-            stream.wait_event(ev_in[i])
-            stream.wait_event(ev_out[i])         # previous step's results have left the device
-            cache.get(L["h"], version[0], True, stream=stream)
-            c = fp.LinearContext(ctx.ctx, N, L["K"])
-            fp.fp8_linear_fwd(L["x"], cache, L["h"], RECIPE, ws=ws, y=L["y"], ctx=c, stream=stream)
-            fp.fp8_linear_bwd(L["dy"], c, cache, L["h"], RECIPE, ws=ws, dx=L["dx"], dw=L["dw"],
-                              stream=stream)
-            ev_done[i].record(stream)
-            s_out.wait_event(ev_done[i])
-            with torch.cuda.stream(s_out):
-                hy.copy_(L["y"], non_blocking=True)
-                hdx.copy_(L["dx"], non_blocking=True)
-                hdw.copy_(L["dw"], non_blocking=True)
-                ev_out[i].record(s_out)
+        for i, L in enumerate(layers):
+            pipe.step(i, host[i], devs[i], ctx, ws, cache, L["h"], RECIPE, version[0])
 
     k = max(3, min(args.steps, 20))
     step()
-    torch.cuda.synchronize()
+    pipe.sync()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     t0.record(stream)
-    s_in.wait_stream(stream)     # no copy of the timed steps starts before t0
-    s_out.wait_stream(stream)
+    pipe.fork(stream)       # no copy or kernel of the timed steps starts before t0
     for _ in range(k):
         step()
-    # the region ends when the last results are on the host
-    for e in ev_out:
-        stream.wait_event(e)
+    pipe.join(stream)       # the region ends when the last results are on the host
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     ms = reduce_max(t0.elapsed_time(t1), world, dev) / k
     value = world * len(SHAPES) * N / (ms / 1e3)
+    link = _link_GBps(dev)
+    copy = (h2d + d2h) / (ms / 1e3) / 1e9
     return {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": k, "ms_per_step": ms,
-            "copy_GBps": (h2d + d2h) / (ms / 1e3) / 1e9,
-            "overlap": "H2D / compute / D2H on three streams"}
+            "copy_GBps": copy, "link_GBps_both_directions": link,
+            "copy_frac_of_link": copy / link if link > 0 else None,
+            "api": "fp8_linear_step_host (host buffers; library copy-in / compute / "
+                   "copy-out streams, one slot per linear)"}
 
 
 def main(argv=None):

@@ -19,7 +19,7 @@ __all__ = [
     "fp8_quantize", "fp8_scale_shape", "fp8_gemm", "fp8_linear_fwd", "fp8_linear_bwd",
     "fp8_gelu_fwd", "fp8_gelu_bwd", "fp8_grad_accumulate", "fp8_get_device_status",
     "fp8_launch_count", "fp8_profile_begin", "fp8_profile_end", "WeightCache", "LinearContext",
-    "fp8_quantize_delayed", "fp8_debug_wait_timeout",
+    "fp8_quantize_delayed", "fp8_debug_wait_timeout", "HostPipeline",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -82,6 +82,27 @@ _SIGS = {
     "fp8_linear_bwd_quantized": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_p, _c_p,
                                           ctypes.c_int32, _c_int, _c_p, _c_p, _c_p, _c_sz, _c_p]),
 }
+
+
+class _HostIO(ctypes.Structure):
+    _fields_ = [("X", _c_p), ("W", _c_p), ("dY", _c_p), ("Y", _c_p), ("dX", _c_p), ("dW", _c_p)]
+
+
+class _DeviceIO(ctypes.Structure):
+    _fields_ = [("X", _c_p), ("dY", _c_p), ("Y", _c_p), ("dX", _c_p), ("dW", _c_p),
+                ("ctx", _c_p), ("ws", _c_p), ("ws_bytes", _c_sz)]
+
+
+_SIGS.update({
+    "fp8_host_pipeline_create": (_c_int, [_c_int, ctypes.POINTER(_c_p)]),
+    "fp8_host_pipeline_destroy": (None, [_c_p]),
+    "fp8_linear_step_host": (_c_int, [_c_p, _c_int, _c_i64, ctypes.POINTER(_HostIO),
+                                      ctypes.POINTER(_DeviceIO), _c_p, ctypes.c_int32, _c_int,
+                                      ctypes.c_uint64]),
+    "fp8_host_pipeline_fork": (_c_int, [_c_p, _c_p]),
+    "fp8_host_pipeline_join": (_c_int, [_c_p, _c_p]),
+    "fp8_host_pipeline_sync": (_c_int, [_c_p]),
+})
 
 
 class _KernelStat(ctypes.Structure):
@@ -490,3 +511,41 @@ def fp8_linear_bwd_quantized(gq: QuantizedTensor, ctx: LinearContext, cache: Wei
                                           h, RECIPE[recipe], _ptr(dx), _ptr(dw), _ptr(ws),
                                           ws.numel(), _stream(stream)), "fp8_linear_bwd_quantized")
     return dx, dw
+
+
+class HostPipeline:
+    """Owns an fp8_host_pipeline: one fwd+bwd of an isolated FP8 linear per
+    step() call, with inputs and results in (pinned) host tensors and the
+    host<->device copies done by the library on its own streams."""
+
+    def __init__(self, slots: int):
+        h = ctypes.c_void_p()
+        _check(lib().fp8_host_pipeline_create(slots, ctypes.byref(h)), "fp8_host_pipeline_create")
+        self._h = h
+
+    def step(self, slot: int, host: dict, dev: dict, ctx: LinearContext, ws: torch.Tensor,
+             cache: WeightCache, h: int, recipe: str, version: int):
+        """host: X, W, dY, Y, dX (or None), dW as CPU bf16 tensors; dev: X, dY, Y,
+        dX (or None), dW as CUDA bf16 tensors (W goes to the buffer registered
+        for handle h)."""
+        N = host["X"].shape[0]
+        hio = _HostIO(*[_ptr(host[k]) for k in ("X", "W", "dY", "Y", "dX", "dW")])
+        dio = _DeviceIO(*[_ptr(dev[k]) for k in ("X", "dY", "Y", "dX", "dW")], _ptr(ctx.ctx),
+                        _ptr(ws), ws.numel())
+        _check(lib().fp8_linear_step_host(self._h, slot, N, ctypes.byref(hio), ctypes.byref(dio),
+                                          cache.handle, h, RECIPE[recipe], version),
+               "fp8_linear_step_host")
+
+    def fork(self, stream=None):
+        _check(lib().fp8_host_pipeline_fork(self._h, _stream(stream)), "fp8_host_pipeline_fork")
+
+    def join(self, stream=None):
+        _check(lib().fp8_host_pipeline_join(self._h, _stream(stream)), "fp8_host_pipeline_join")
+
+    def sync(self):
+        _check(lib().fp8_host_pipeline_sync(self._h), "fp8_host_pipeline_sync")
+
+    def __del__(self):
+        if getattr(self, "_h", None) is not None and _lib is not None:
+            _lib.fp8_host_pipeline_destroy(self._h)
+            self._h = None

@@ -662,6 +662,139 @@ fp8_status fp8_profile_end(fp8_kernel_stat *out, int cap, int *n) {
   return st;
 }
 
+// ---------------------------------------------------------------- host-buffer steps
+struct fp8_host_pipeline {
+  int device = 0;
+  cudaStream_t copy_in = nullptr, compute = nullptr, copy_out = nullptr;
+  struct Slot {
+    cudaEvent_t in_done = nullptr;       // this slot's inputs are on the device
+    cudaEvent_t compute_done = nullptr;  // this slot's kernels have finished
+    cudaEvent_t out_done = nullptr;      // this slot's results are on the host
+  };
+  std::vector<Slot> slots;
+  cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
+};
+
+void fp8_host_pipeline_destroy(fp8_host_pipeline *p) {
+  if (!p) return;
+  for (auto &s : p->slots)
+    for (cudaEvent_t e : {s.in_done, s.compute_done, s.out_done})
+      if (e) cudaEventDestroy(e);
+  for (cudaEvent_t e : {p->fork_ev, p->join_ev})
+    if (e) cudaEventDestroy(e);
+  for (cudaStream_t s : {p->copy_in, p->compute, p->copy_out})
+    if (s) cudaStreamDestroy(s);
+  delete p;
+}
+
+fp8_status fp8_host_pipeline_create(int slots, fp8_host_pipeline **out) {
+  if (!out || slots <= 0 || slots > 4096) return FP8_ERR_INVALID_ARG;
+  *out = nullptr;
+  auto *p = new (std::nothrow) fp8_host_pipeline();
+  if (!p) return FP8_ERR_INVALID_ARG;
+  bool ok = cudaGetDevice(&p->device) == cudaSuccess;
+  for (cudaStream_t *s : {&p->copy_in, &p->compute, &p->copy_out})
+    ok = ok && cudaStreamCreateWithFlags(s, cudaStreamNonBlocking) == cudaSuccess;
+  p->slots.resize((size_t)slots);
+  for (auto &s : p->slots)
+    for (cudaEvent_t *e : {&s.in_done, &s.compute_done, &s.out_done})
+      ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+  for (cudaEvent_t *e : {&p->fork_ev, &p->join_ev})
+    ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    fp8_host_pipeline_destroy(p);
+    return FP8_ERR_CUDA;
+  }
+  *out = p;
+  return FP8_OK;
+}
+
+fp8_status fp8_linear_step_host(fp8_host_pipeline *p, int slot, int64_t N,
+                                const fp8_linear_host_io *host, const fp8_linear_device_io *dev,
+                                fp8_weight_cache *cache, fp8_weight_handle h, fp8_recipe recipe,
+                                uint64_t w_version) {
+  // every check the enqueued calls would make, before anything is enqueued
+  if (!p || slot < 0 || (size_t)slot >= p->slots.size() || !host || !dev || !cache || h < 0 ||
+      (size_t)h >= cache->entries.size() || !valid_linear_recipe(recipe))
+    return FP8_ERR_INVALID_ARG;
+  const auto &e = cache->entries[h];
+  if (e.recipe != recipe) return FP8_ERR_INVALID_ARG;
+  const int64_t K = e.K, O = e.O;
+  fp8_status st = check_dims(N, K);
+  if (st != FP8_OK) return st;
+  if (N == 0) return FP8_OK;
+  if (!host->X || !host->W || !host->dY || !host->Y || !host->dW || !dev->X || !dev->dY ||
+      !dev->Y || !dev->dW || !dev->ctx || !dev->ws)
+    return FP8_ERR_INVALID_ARG;
+  if (!aligned16(dev->X) || !aligned16(dev->dY) || !aligned16(dev->Y) || !aligned16(dev->dW) ||
+      !aligned16(dev->ctx) || !aligned16(dev->ws) || (dev->dX && !aligned16(dev->dX)))
+    return FP8_ERR_ALIGN;
+  size_t need = 0;
+  fp8_linear_workspace_size(recipe, N, K, O, &need);
+  if (dev->ws_bytes < need) return FP8_ERR_WORKSPACE;
+  if (e.cycle == cache->cycle && e.version != w_version) return FP8_ERR_STALE;
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != p->device) return FP8_ERR_INVALID_ARG;
+
+  auto &s = p->slots[(size_t)slot];
+  const size_t xb = (size_t)N * K * 2, wb = (size_t)O * K * 2, gb = (size_t)N * O * 2;
+  bool ok = cudaStreamWaitEvent(p->copy_in, s.compute_done, 0) == cudaSuccess &&
+            cudaMemcpyAsync(dev->X, host->X, xb, cudaMemcpyHostToDevice, p->copy_in) ==
+                cudaSuccess &&
+            cudaMemcpyAsync(const_cast<void *>(e.w), host->W, wb, cudaMemcpyHostToDevice,
+                            p->copy_in) == cudaSuccess &&
+            cudaMemcpyAsync(dev->dY, host->dY, gb, cudaMemcpyHostToDevice, p->copy_in) ==
+                cudaSuccess &&
+            cudaEventRecord(s.in_done, p->copy_in) == cudaSuccess &&
+            cudaStreamWaitEvent(p->compute, s.in_done, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(p->compute, s.out_done, 0) == cudaSuccess;
+  if (!ok) return FP8_ERR_CUDA;
+  fp8_stream_t cst = reinterpret_cast<fp8_stream_t>(p->compute);
+  st = fp8_weight_cache_get(cache, h, w_version, 1, cst, nullptr);
+  if (st == FP8_OK)
+    st = fp8_linear_fwd(dev->X, N, K, cache, h, recipe, dev->Y, dev->ctx, dev->ws, dev->ws_bytes,
+                        cst);
+  if (st == FP8_OK)
+    st = fp8_linear_bwd(dev->dY, N, O, dev->ctx, cache, h, recipe, dev->dX, dev->dW, dev->ws,
+                        dev->ws_bytes, cst);
+  if (st != FP8_OK) return st;
+  ok = cudaEventRecord(s.compute_done, p->compute) == cudaSuccess &&
+       cudaStreamWaitEvent(p->copy_out, s.compute_done, 0) == cudaSuccess &&
+       cudaMemcpyAsync(host->Y, dev->Y, gb, cudaMemcpyDeviceToHost, p->copy_out) == cudaSuccess &&
+       (!host->dX || !dev->dX ||
+        cudaMemcpyAsync(host->dX, dev->dX, xb, cudaMemcpyDeviceToHost, p->copy_out) ==
+            cudaSuccess) &&
+       cudaMemcpyAsync(host->dW, dev->dW, wb, cudaMemcpyDeviceToHost, p->copy_out) ==
+           cudaSuccess &&
+       cudaEventRecord(s.out_done, p->copy_out) == cudaSuccess;
+  return ok ? FP8_OK : FP8_ERR_CUDA;
+}
+
+fp8_status fp8_host_pipeline_fork(fp8_host_pipeline *p, fp8_stream_t s) {
+  if (!p) return FP8_ERR_INVALID_ARG;
+  bool ok = cudaEventRecord(p->fork_ev, cs(s)) == cudaSuccess;
+  for (cudaStream_t t : {p->copy_in, p->compute, p->copy_out})
+    ok = ok && cudaStreamWaitEvent(t, p->fork_ev, 0) == cudaSuccess;
+  return ok ? FP8_OK : FP8_ERR_CUDA;
+}
+
+fp8_status fp8_host_pipeline_join(fp8_host_pipeline *p, fp8_stream_t s) {
+  if (!p) return FP8_ERR_INVALID_ARG;
+  bool ok = true;
+  for (cudaStream_t t : {p->copy_in, p->compute, p->copy_out})
+    ok = ok && cudaEventRecord(p->join_ev, t) == cudaSuccess &&
+         cudaStreamWaitEvent(cs(s), p->join_ev, 0) == cudaSuccess;
+  return ok ? FP8_OK : FP8_ERR_CUDA;
+}
+
+fp8_status fp8_host_pipeline_sync(fp8_host_pipeline *p) {
+  if (!p) return FP8_ERR_INVALID_ARG;
+  bool ok = true;
+  for (cudaStream_t t : {p->copy_in, p->compute, p->copy_out})
+    ok = ok && cudaStreamSynchronize(t) == cudaSuccess;
+  return ok ? FP8_OK : FP8_ERR_CUDA;
+}
+
 fp8_status fp8_debug_wait_timeout(uint64_t limit_ns, fp8_stream_t stream) {
   if (limit_ns == 0 || limit_ns > 1000000000ull) return FP8_ERR_INVALID_ARG;
   return from_cuda(launch_wait_timeout_probe(limit_ns, cs(stream)));

@@ -291,6 +291,62 @@ fp8_status fp8_gelu_fwd(const void *H, void *A, int64_t n, fp8_stream_t stream);
 fp8_status fp8_gelu_bwd(const void *dA, const void *H, void *dH, int64_t n, fp8_stream_t stream);
 fp8_status fp8_grad_accumulate(float *acc, const void *dW, int64_t n, fp8_stream_t stream);
 
+/* ------------------------------------------------------------------ host-buffer steps
+ * One forward + backward of an isolated FP8 linear (fp8_linear_fwd then
+ * fp8_linear_bwd, same recipe rules) whose inputs and results live in HOST
+ * memory: the library copies them to and from the caller's device buffers.
+ * Host buffers should be page-locked (cudaHostAlloc / pinned): pageable
+ * memory works but then the copies stage through the driver and block.
+ *
+ * A pipeline owns three CUDA streams on the device current at creation
+ * (copy-in, compute, copy-out) and `slots` sets of events.  Each slot stands
+ * for one set of device buffers (one linear).  fp8_linear_step_host(slot):
+ *   copy-in:  X, W, dY host -> device (W into the buffer registered for the
+ *             weight handle), after this slot's previous compute has finished
+ *             reading them;
+ *   compute:  fp8_weight_cache_get(h, w_version, use_cache = 1), then
+ *             fp8_linear_fwd and fp8_linear_bwd, after this slot's copy-in
+ *             and after this slot's previous results have left the device;
+ *   copy-out: Y, dX (if both pointers are set), dW device -> host.
+ * Calls on different slots overlap: the copies of one linear run while
+ * another's kernels execute.  The compute work of all slots is ordered on the
+ * one compute stream, so `ctx` and `ws` may be shared by all slots; the
+ * weight handle of a slot must not be used by another slot.  The call
+ * returns once everything is enqueued; results are on the host after
+ * fp8_host_pipeline_sync (or after fp8_host_pipeline_join on a stream that
+ * is then synchronised).
+ *   fp8_host_pipeline_fork(p, s): the pipeline's streams wait for the work
+ *     enqueued on s so far (an event recorded on s before marks a start).
+ *   fp8_host_pipeline_join(p, s): s waits for all work enqueued on the
+ *     pipeline so far (an event recorded on s afterwards marks the end).
+ * Errors: INVALID_ARG (null pipeline, slot out of range, null buffer, handle
+ * or recipe mismatch), SHAPE, ALIGN (device buffers), STALE, WORKSPACE, CUDA.
+ * Nothing is enqueued when a check fails. */
+typedef struct fp8_host_pipeline fp8_host_pipeline;
+typedef struct {
+  const void *X;  /* [N, K] bf16 */
+  const void *W;  /* [O, K] bf16 */
+  const void *dY; /* [N, O] bf16 */
+  void *Y;        /* [N, O] bf16 */
+  void *dX;       /* [N, K] bf16, or NULL (no dgrad copy-back) */
+  void *dW;       /* [O, K] bf16 */
+} fp8_linear_host_io;
+typedef struct {
+  void *X, *dY, *Y, *dX, *dW; /* device buffers of the slot (dX may be NULL: no dgrad) */
+  void *ctx;                  /* fp8_linear_ctx_size bytes */
+  void *ws;                   /* fp8_linear_workspace_size bytes */
+  size_t ws_bytes;
+} fp8_linear_device_io;
+fp8_status fp8_host_pipeline_create(int slots, fp8_host_pipeline **out);
+void fp8_host_pipeline_destroy(fp8_host_pipeline *p);
+fp8_status fp8_linear_step_host(fp8_host_pipeline *p, int slot, int64_t N,
+                                const fp8_linear_host_io *host, const fp8_linear_device_io *dev,
+                                fp8_weight_cache *cache, fp8_weight_handle h, fp8_recipe recipe,
+                                uint64_t w_version);
+fp8_status fp8_host_pipeline_fork(fp8_host_pipeline *p, fp8_stream_t s);
+fp8_status fp8_host_pipeline_join(fp8_host_pipeline *p, fp8_stream_t s);
+fp8_status fp8_host_pipeline_sync(fp8_host_pipeline *p);
+
 /* ------------------------------------------------------------------ kernel timing
  * Per-kernel timing for roofline reports.  Between fp8_profile_begin and
  * fp8_profile_end every kernel this library launches is bracketed by two

@@ -102,3 +102,18 @@ def test_weight_cache_bookkeeping_without_gpu(L):
     assert L.fp8_weight_cache_begin_cycle(c) == 0
     assert L.fp8_launch_count() == n0
     L.fp8_weight_cache_destroy(c)
+
+
+def test_host_pipeline_validation_without_gpu(L):
+    P = ctypes.c_void_p
+    p = P()
+    assert L.fp8_host_pipeline_create(0, ctypes.byref(p)) == 1
+    assert L.fp8_host_pipeline_create(2, None) == 1
+    # no pipeline: every call is refused before anything is enqueued
+    n0 = L.fp8_launch_count()
+    assert L.fp8_linear_step_host(None, 0, 128, None, None, None, 0, 0, 1) == 1
+    assert L.fp8_host_pipeline_fork(None, None) == 1
+    assert L.fp8_host_pipeline_join(None, None) == 1
+    assert L.fp8_host_pipeline_sync(None) == 1
+    L.fp8_host_pipeline_destroy(None)
+    assert L.fp8_launch_count() == n0
