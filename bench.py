@@ -391,6 +391,39 @@ def run_mlp_workloads(fp, dev, stream):
     same = same and all(torch.equal(a.view(torch.int32), b.view(torch.int32))
                         for a, b in zip(grads[False], grads[True]))
     med = {k: statistics.median(v) for k, v in times.items()}
+    # the same steps captured once per mode in a CUDA graph and replayed, so
+    # host launch jitter cannot swamp a difference of a few tenths of a percent
+    graphs = {}
+    for use in (False, True):
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):       # warm the capture stream's allocator
+            stk.step(xs, dys, use, keep_outputs=False)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            stk.step(xs, dys, use, keep_outputs=False)
+        graphs[use] = g
+    gtimes = {False: [], True: []}
+    for _ in range(5):                      # 5 interleaved groups of 2 replays per mode
+        for use in (False, True):
+            gtimes[use].append(timed(graphs[use].replay, 2))
+    gmed = {k: statistics.median(v) for k, v in gtimes.items()}
+    del graphs
+    # what caching skips: one weight quantization of each fc1 / fc2 shape
+    # (device time of its kernels from the library's per-kernel events)
+    wq = {}
+    for name, (O, K) in (("fc1", (ffn, d)), ("fc2", (d, ffn))):
+        wt = syn.bf16_normal((O, K), 0.02, 900, device=dev)
+        fp.fp8_quantize(wt, "block", "weight")
+        torch.cuda.synchronize()
+        fp.fp8_profile_begin()
+        for _ in range(50):
+            fp.fp8_quantize(wt, "block", "weight")
+        torch.cuda.synchronize()
+        wq[name] = sum(k["total_ms"] for k in fp.fp8_profile_end()) / 50
+    skipped = (GA - 1) * L * (wq["fc1"] + wq["fc2"])
     out["weight_cache_stack"] = {
         "workload": "8-layer MLP stack (16 FP8 linears, d=512, ffn=2048), GA=4 x 131072 tokens, "
                     "block scaling",
@@ -399,7 +432,14 @@ def run_mlp_workloads(fp, dev, stream):
         "samples_uncached": times[False], "samples_cached": times[True],
         "bitwise_identical": bool(same),
         "weight_quantizations_per_step": {"uncached": 2 * L * GA, "cached": 2 * L},
-        "tokens_per_s_cached": GA * N / (med[True] / 1e3)}
+        "tokens_per_s_cached": GA * N / (med[True] / 1e3),
+        "graph_replay": {
+            "ms_per_step_uncached": gmed[False], "ms_per_step_cached": gmed[True],
+            "reduction_pct": 100.0 * (gmed[False] - gmed[True]) / gmed[False],
+            "groups_uncached": gtimes[False], "groups_cached": gtimes[True]},
+        "weight_quantize_ms": wq,
+        "skipped_weight_quantize_ms_per_step": skipped,
+        "skipped_pct_of_uncached_step": 100.0 * skipped / gmed[False]}
     del stk, xs, dys, res, grads
     torch.cuda.empty_cache()
 
