@@ -314,19 +314,33 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
     if (MODE != Q_TENSOR) {
       uint32_t tm = 0;              // 128x128: running tile maximum (pair)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = rr + 16 * i;
-        const uint4 w = xw[i];
+      for (int i = 0; i < 8; i += 2) {
         if (MODE == Q_BLOCK1x128) {
-          cm[0] = absmax2(cm[0], w.x); cm[1] = absmax2(cm[1], w.y);
-          cm[2] = absmax2(cm[2], w.z); cm[3] = absmax2(cm[3], w.w);
-          uint32_t rm = absmax2(absmax2(absmax2(absmax2(0u, w.x), w.y), w.z), w.w);
-          float a = bf16pair_max(rm);
+          // rows rr+16i and rr+16(i+1): each row's maximum over this thread's
+          // 8 columns, the two packed as one bf16 pair, reduced over the 16
+          // lanes of the row group with 4 shuffles for both rows at once
+          uint32_t m2[2];
 #pragma unroll
-          for (int o = 1; o < 16; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-          if (cg == 0) S.rowmx[r] = a;
+          for (int h = 0; h < 2; ++h) {
+            const uint4 w = xw[i + h];
+            cm[0] = absmax2(cm[0], w.x); cm[1] = absmax2(cm[1], w.y);
+            cm[2] = absmax2(cm[2], w.z); cm[3] = absmax2(cm[3], w.w);
+            const uint32_t rm = absmax2(absmax2(absmax2(absmax2(0u, w.x), w.y), w.z), w.w);
+            m2[h] = absmax2(rm, __byte_perm(rm, rm, 0x1032));  // both halves = row max
+          }
+          uint32_t pr = __byte_perm(m2[0], m2[1], 0x7610);  // lo: row i, hi: row i+1
+#pragma unroll
+          for (int o = 1; o < 16; o <<= 1) pr = absmax2(pr, __shfl_xor_sync(0xffffffffu, pr, o));
+          if (cg == 0) {
+            S.rowmx[rr + 16 * i] = __uint_as_float(pr << 16);
+            S.rowmx[rr + 16 * (i + 1)] = __uint_as_float(pr & 0xFFFF0000u);
+          }
         } else {
-          tm = absmax2(absmax2(absmax2(absmax2(tm, w.x), w.y), w.z), w.w);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint4 w = xw[i + h];
+            tm = absmax2(absmax2(absmax2(absmax2(tm, w.x), w.y), w.z), w.w);
+          }
         }
       }
       if (MODE == Q_BLOCK128) {
