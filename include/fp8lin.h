@@ -20,8 +20,9 @@
  *     W is [O, K] (out x in), Y = X W^T is [N, O].  A "colwise" or
  *     "transposed" layout of an [R, C] tensor is the [C, R] array, row-major.
  *   - Every tensor pointer is a DEVICE pointer owned by the caller, 16-byte
- *     aligned.  The library allocates no device memory; scratch space is the
- *     caller's `workspace` (size from the *_workspace_size queries).
+ *     aligned, except the host buffers of fp8_linear_step_host.  The library
+ *     allocates no device memory; scratch space is the caller's `workspace`
+ *     (size from the *_workspace_size queries).
  *   - Every dimension must be a multiple of 16 (TMA row-stride rule).  A
  *     dimension need not be a multiple of 128: the last 128-block of a row,
  *     column or tile is then shorter ("ragged tail") and its amax covers the
@@ -29,7 +30,8 @@
  *   - bf16 tensors are passed as `const void*` (IEEE bfloat16 bit patterns).
  *   - Every call enqueues work on `stream` (a cudaStream_t; NULL = legacy
  *     default stream) and returns without synchronising, except
- *     fp8_get_device_status.  Arguments are validated before anything is
+ *     fp8_get_device_status and fp8_host_pipeline_sync (fp8_linear_step_host
+ *     enqueues on its pipeline's own streams).  Arguments are validated before anything is
  *     launched: on a non-OK status nothing was enqueued.
  *   - Calls are not thread-safe with respect to one fp8_weight_cache object.
  *
