@@ -205,7 +205,7 @@ def run_ours(args):
                for L in layers), key=lambda c: c.ctx.numel())
     version = [0]
 
-    def step():
+    def step_serial():
         cache.begin_cycle()
         version[0] += 1
         for L in layers:
@@ -214,30 +214,84 @@ def run_ours(args):
             fp.fp8_linear_fwd(L["x"], cache, L["h"], RECIPE, ws=ws, y=L["y"], ctx=c)
             fp.fp8_linear_bwd(L["dy"], c, cache, L["h"], RECIPE, ws=ws, dx=L["dx"], dw=L["dw"])
 
+    # The same work with the tensorwise amax passes of X and dY (pure HBM
+    # reads, almost no shared memory) on a second stream, where their CTAs run
+    # beside the GEMM and cast CTAs of earlier linears; each cast waits for its
+    # tensor's partial maxima.  Results are bit for bit those of step_serial.
     stream = torch.cuda.current_stream()
-    for _ in range(args.warmup):
-        step()
+    aux = torch.cuda.Stream(dev)
+    px = [fp.amax_partials_buffer(N, L["K"], dev) for L in layers]
+    pdy = [fp.amax_partials_buffer(N, L["O"], dev) for L in layers]
+    ev_go = torch.cuda.Event()
+    ev_x = [torch.cuda.Event() for _ in layers]
+    ev_dy = [torch.cuda.Event() for _ in layers]
+
+    def step_overlap():
+        cache.begin_cycle()
+        version[0] += 1
+        ev_go.record(stream)          # earlier casts are done with the partial buffers
+        aux.wait_event(ev_go)
+        with torch.cuda.stream(aux):
+            for i, L in enumerate(layers):
+                fp.fp8_amax_partials(L["x"], px[i])
+                ev_x[i].record(aux)
+                fp.fp8_amax_partials(L["dy"], pdy[i])
+                ev_dy[i].record(aux)
+        for i, L in enumerate(layers):
+            cache.get(L["h"], version[0], True)
+            c = fp.LinearContext(ctx.ctx, N, L["K"])
+            stream.wait_event(ev_x[i])
+            fp.fp8_linear_fwd_after_amax(L["x"], px[i], cache, L["h"], RECIPE, ws, L["y"], c)
+            stream.wait_event(ev_dy[i])
+            fp.fp8_linear_bwd_after_amax(L["dy"], pdy[i], c, cache, L["h"], RECIPE, ws, L["dx"],
+                                         L["dw"])
+
+    step = step_overlap if args.schedule == "overlap" else step_serial
+    for _ in range(args.warmup):        # both schedules, so either can be timed warm
+        step_overlap()
+        step_serial()
     torch.cuda.synchronize()
     st = fp.fp8_get_device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} after warm-up")
 
-    # ---- device-resident timing
+    # ---- device-resident timing: `value` comes from K steps with no per-kernel
+    # events (recording two events around every launch costs a few percent of
+    # the step); the per-kernel times for the roofline come from K more steps
+    # of the same work with the library's events on.
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier(world)
         torch.cuda.synchronize()
         n_launch0 = fp.fp8_launch_count()
-        fp.fp8_profile_begin()
         t0.record(stream)
         for _ in range(args.steps):
             step()
         t1.record(stream)
         torch.cuda.synchronize()
         barrier(world)
-        kstats = fp.fp8_profile_end()
         n_launch = fp.fp8_launch_count() - n_launch0
     clocks = clk.summary()
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    fp.fp8_profile_begin()
+    p0.record(stream)
+    for _ in range(args.steps):
+        step()
+    p1.record(stream)
+    torch.cuda.synchronize()
+    kstats = fp.fp8_profile_end()
+    profiled_ms_step = p0.elapsed_time(p1) / args.steps
+    # the other schedule, for reference (same work, same results)
+    other = step_serial if args.schedule == "overlap" else step_overlap
+    o0, o1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    o0.record(stream)
+    for _ in range(args.steps):
+        other()
+    o1.record(stream)
+    torch.cuda.synchronize()
+    other_ms_step = reduce_max(o0.elapsed_time(o1), world, dev) / args.steps
     ms_local = t0.elapsed_time(t1)
     ms_total = reduce_max(ms_local, world, dev)
     ms_step = ms_total / args.steps
@@ -272,6 +326,8 @@ def run_ours(args):
     roof["peak_source"] = peaks["source"] + (" sustained bf16 x 2" if roof["bound"] == "tensor"
                                              else " copy bandwidth")
     roof["traffic"] = _traffic_for(dom["name"])
+    roof["timing"] = ("CUDA events around each launch on its stream, over a second region of "
+                      "the same K steps (value comes from an event-free region)")
 
     # ---- end to end through the C ABI with host buffers
     e2e = run_e2e(fp, layers, cache, ws, ctx, N, dev, world, args, stream)
@@ -309,7 +365,13 @@ def run_ours(args):
                                    "scaling, fused dual-layout casts, weight quantized every step",
                        "tokens_per_step": tokens_per_step, "recipe": RECIPE,
                        "l2": "inputs larger than L2 (about 9 GB touched per step)",
-                       "parallelism": f"dp{world} (replicas, no collective)"},
+                       "parallelism": f"dp{world} (replicas, no collective)",
+                       "schedule": ("tensorwise amax passes on a second stream beside the "
+                                    "GEMMs and casts" if args.schedule == "overlap"
+                                    else "one stream")},
+            "other_schedule_ms_per_step": {("serial" if args.schedule == "overlap"
+                                            else "overlap"): other_ms_step},
+            "profiled_ms_per_step": profiled_ms_step,
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
@@ -689,6 +751,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--schedule", choices=["serial", "overlap"], default="serial",
+                    help="overlap: tensorwise amax passes on a second stream")
     ap.add_argument("--no-mlp", action="store_true",
                     help="skip the MLP-level workloads reported beside the main line")
     args = ap.parse_args(argv)

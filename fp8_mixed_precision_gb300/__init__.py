@@ -19,7 +19,8 @@ __all__ = [
     "fp8_quantize", "fp8_scale_shape", "fp8_gemm", "fp8_linear_fwd", "fp8_linear_bwd",
     "fp8_gelu_fwd", "fp8_gelu_bwd", "fp8_grad_accumulate", "fp8_get_device_status",
     "fp8_launch_count", "fp8_profile_begin", "fp8_profile_end", "WeightCache", "LinearContext",
-    "fp8_quantize_delayed", "fp8_debug_wait_timeout", "HostPipeline",
+    "fp8_quantize_delayed", "fp8_debug_wait_timeout", "HostPipeline", "amax_partials_buffer",
+    "fp8_amax_partials", "fp8_linear_fwd_after_amax", "fp8_linear_bwd_after_amax",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -94,6 +95,11 @@ class _DeviceIO(ctypes.Structure):
 
 
 _SIGS.update({
+    "fp8_amax_partials": (_c_int, [_c_p, _c_i64, _c_i64, _c_p, _c_sz, _c_p]),
+    "fp8_linear_fwd_after_amax": (_c_int, [_c_p, _c_p, _c_i64, _c_i64, _c_p, ctypes.c_int32, _c_int,
+                                           _c_p, _c_p, _c_p, _c_sz, _c_p]),
+    "fp8_linear_bwd_after_amax": (_c_int, [_c_p, _c_p, _c_i64, _c_i64, _c_p, _c_p, ctypes.c_int32,
+                                           _c_int, _c_p, _c_p, _c_p, _c_sz, _c_p]),
     "fp8_host_pipeline_create": (_c_int, [_c_int, ctypes.POINTER(_c_p)]),
     "fp8_host_pipeline_destroy": (None, [_c_p]),
     "fp8_linear_step_host": (_c_int, [_c_p, _c_int, _c_i64, ctypes.POINTER(_HostIO),
@@ -549,3 +555,43 @@ class HostPipeline:
         if getattr(self, "_h", None) is not None and _lib is not None:
             _lib.fp8_host_pipeline_destroy(self._h)
             self._h = None
+
+
+def amax_partials_buffer(rows: int, cols: int, device) -> torch.Tensor:
+    """Device buffer for fp8_amax_partials of a [rows, cols] tensor."""
+    return _empty_bytes(_quant_ws_bytes("tensorwise", rows, cols), device)
+
+
+def fp8_amax_partials(x: torch.Tensor, partials: torch.Tensor, stream=None) -> torch.Tensor:
+    """First tensorwise pass alone (per-CTA maxima of |x|) into `partials`."""
+    _need_bf16_cuda(x, "x")
+    R, C = x.shape
+    _check(lib().fp8_amax_partials(_ptr(x), R, C, _ptr(partials), partials.numel(),
+                                   _stream(stream)), "fp8_amax_partials")
+    return partials
+
+
+def fp8_linear_fwd_after_amax(x: torch.Tensor, x_partials: torch.Tensor, cache: WeightCache,
+                              h: int, recipe: str, ws: torch.Tensor, y: torch.Tensor,
+                              ctx: LinearContext, stream=None):
+    """fp8_linear_fwd with X's amax pass already run by fp8_amax_partials."""
+    _need_bf16_cuda(x, "x")
+    N, K = x.shape
+    _check(lib().fp8_linear_fwd_after_amax(_ptr(x), _ptr(x_partials), N, K, cache.handle, h,
+                                           RECIPE[recipe], _ptr(y), _ptr(ctx.ctx), _ptr(ws),
+                                           ws.numel(), _stream(stream)),
+           "fp8_linear_fwd_after_amax")
+    return y, ctx
+
+
+def fp8_linear_bwd_after_amax(dy: torch.Tensor, dy_partials: torch.Tensor, ctx: LinearContext,
+                              cache: WeightCache, h: int, recipe: str, ws: torch.Tensor,
+                              dx: torch.Tensor | None, dw: torch.Tensor, stream=None):
+    """fp8_linear_bwd with dY's amax pass already run by fp8_amax_partials."""
+    _need_bf16_cuda(dy, "dy")
+    N, O = dy.shape
+    _check(lib().fp8_linear_bwd_after_amax(_ptr(dy), _ptr(dy_partials), N, O, _ptr(ctx.ctx),
+                                           cache.handle, h, RECIPE[recipe], _ptr(dx), _ptr(dw),
+                                           _ptr(ws), ws.numel(), _stream(stream)),
+           "fp8_linear_bwd_after_amax")
+    return dx, dw

@@ -398,9 +398,13 @@ fp8_status fp8_linear_workspace_size(fp8_recipe recipe, int64_t N, int64_t K, in
   return FP8_OK;
 }
 
-fp8_status fp8_linear_fwd(const void *X, int64_t N, int64_t K, fp8_weight_cache *cache,
-                          fp8_weight_handle h, fp8_recipe recipe, void *Y, void *ctx, void *ws,
-                          size_t ws_bytes, fp8_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// x_partials: the tensorwise first pass over X already ran (fp8_amax_partials)
+fp8_status linear_fwd_impl(const void *X, int64_t N, int64_t K, fp8_weight_cache *cache,
+                           fp8_weight_handle h, fp8_recipe recipe, void *Y, void *ctx, void *ws,
+                           size_t ws_bytes, fp8_stream_t stream, const float *x_partials) {
   if (!cache || h < 0 || (size_t)h >= cache->entries.size() || !valid_linear_recipe(recipe))
     return FP8_ERR_INVALID_ARG;
   const auto &e = cache->entries[h];
@@ -425,18 +429,28 @@ fp8_status fp8_linear_fwd(const void *X, int64_t N, int64_t K, fp8_weight_cache 
   float *rsi = w.take<float>((size_t)ns * 4);
   float *part = w.take<float>(qws);
   void *gws = w.take<void>(gemm_workspace_bytes(N, O, K, fwd_scaling(recipe)));
-  st = fp8_quantize(X, N, K, ar, FP8_ROLE_ACT, xq_row, c + L.xq_col, rs, rsi,
-                    reinterpret_cast<float *>(c + L.scale), reinterpret_cast<float *>(c + L.scale_inv),
-                    part, qws, stream);
+  if (x_partials) {
+    if (ar != FP8_RECIPE_TENSORWISE) return FP8_ERR_UNSUPPORTED;
+    st = from_cuda(launch_quantize(X, N, K, 0, FP8_FORMAT_E4M3, xq_row, c + L.xq_col, rs, rsi,
+                                   reinterpret_cast<float *>(c + L.scale),
+                                   reinterpret_cast<float *>(c + L.scale_inv),
+                                   const_cast<float *>(x_partials), cs(stream), true));
+  } else {
+    st = fp8_quantize(X, N, K, ar, FP8_ROLE_ACT, xq_row, c + L.xq_col, rs, rsi,
+                      reinterpret_cast<float *>(c + L.scale),
+                      reinterpret_cast<float *>(c + L.scale_inv), part, qws, stream);
+  }
   if (st != FP8_OK) return st;
   return fp8_gemm(xq_row, FP8_FORMAT_E4M3, rsi, e.w_row, FP8_FORMAT_E4M3, e.row_scale_inv, N, O, K,
                   fwd_scaling(recipe), Y, gws, gemm_workspace_bytes(N, O, K, fwd_scaling(recipe)),
                   stream);
 }
 
-fp8_status fp8_linear_bwd(const void *dY, int64_t N, int64_t O, const void *ctx,
-                          fp8_weight_cache *cache, fp8_weight_handle h, fp8_recipe recipe, void *dX,
-                          void *dW, void *ws, size_t ws_bytes, fp8_stream_t stream) {
+// dy_partials: the tensorwise first pass over dY already ran (fp8_amax_partials)
+fp8_status linear_bwd_impl(const void *dY, int64_t N, int64_t O, const void *ctx,
+                           fp8_weight_cache *cache, fp8_weight_handle h, fp8_recipe recipe,
+                           void *dX, void *dW, void *ws, size_t ws_bytes, fp8_stream_t stream,
+                           const float *dy_partials) {
   if (!cache || h < 0 || (size_t)h >= cache->entries.size() || !valid_linear_recipe(recipe))
     return FP8_ERR_INVALID_ARG;
   const auto &e = cache->entries[h];
@@ -469,8 +483,14 @@ fp8_status fp8_linear_bwd(const void *dY, int64_t N, int64_t O, const void *ctx,
   float *gcsi = w.take<float>((size_t)nc * 4);
   float *part = w.take<float>(qws);
   void *gws = w.take<void>(gbytes);
-  st = fp8_quantize(dY, N, O, ar, FP8_ROLE_GRAD, g_row, g_col, grs, grsi, gcs, gcsi, part, qws,
-                    stream);
+  if (dy_partials) {
+    if (ar != FP8_RECIPE_TENSORWISE) return FP8_ERR_UNSUPPORTED;
+    st = from_cuda(launch_quantize(dY, N, O, 0, FP8_FORMAT_E5M2, g_row, g_col, grs, grsi, gcs,
+                                   gcsi, const_cast<float *>(dy_partials), cs(stream), true));
+  } else {
+    st = fp8_quantize(dY, N, O, ar, FP8_ROLE_GRAD, g_row, g_col, grs, grsi, gcs, gcsi, part, qws,
+                      stream);
+  }
   if (st != FP8_OK) return st;
   if (dX) {
     st = fp8_gemm(g_row, FP8_FORMAT_E5M2, grsi, e.w_col, FP8_FORMAT_E4M3, e.col_scale_inv, N, K, O,
@@ -480,6 +500,54 @@ fp8_status fp8_linear_bwd(const void *dY, int64_t N, int64_t O, const void *ctx,
   return fp8_gemm(g_col, FP8_FORMAT_E5M2, gcsi, c + L.xq_col, FP8_FORMAT_E4M3,
                   reinterpret_cast<const float *>(c + L.scale_inv), O, K, N, wgrad_scaling(recipe),
                   dW, gws, gbytes, stream);
+}
+}  // namespace
+
+extern "C" {
+
+fp8_status fp8_linear_fwd(const void *X, int64_t N, int64_t K, fp8_weight_cache *cache,
+                          fp8_weight_handle h, fp8_recipe recipe, void *Y, void *ctx, void *ws,
+                          size_t ws_bytes, fp8_stream_t stream) {
+  return linear_fwd_impl(X, N, K, cache, h, recipe, Y, ctx, ws, ws_bytes, stream, nullptr);
+}
+
+fp8_status fp8_linear_bwd(const void *dY, int64_t N, int64_t O, const void *ctx,
+                          fp8_weight_cache *cache, fp8_weight_handle h, fp8_recipe recipe, void *dX,
+                          void *dW, void *ws, size_t ws_bytes, fp8_stream_t stream) {
+  return linear_bwd_impl(dY, N, O, ctx, cache, h, recipe, dX, dW, ws, ws_bytes, stream, nullptr);
+}
+
+fp8_status fp8_amax_partials(const void *x, int64_t rows, int64_t cols, void *partials,
+                             size_t partials_bytes, fp8_stream_t stream) {
+  fp8_status st = check_dims(rows, cols);
+  if (st != FP8_OK) return st;
+  if (rows == 0 || cols == 0) return FP8_OK;
+  if (!x || !partials) return FP8_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(partials)) return FP8_ERR_ALIGN;
+  size_t need = 0;
+  fp8_quantize_workspace_size(FP8_RECIPE_TENSORWISE, rows, cols, &need);
+  if (partials_bytes < need) return FP8_ERR_WORKSPACE;
+  return from_cuda(launch_amax_partials(x, rows, cols, static_cast<float *>(partials), cs(stream)));
+}
+
+fp8_status fp8_linear_fwd_after_amax(const void *X, const void *x_partials, int64_t N, int64_t K,
+                                     fp8_weight_cache *cache, fp8_weight_handle h,
+                                     fp8_recipe recipe, void *Y, void *ctx, void *ws,
+                                     size_t ws_bytes, fp8_stream_t stream) {
+  if (!x_partials && N > 0) return FP8_ERR_INVALID_ARG;
+  if (x_partials && !aligned16(x_partials)) return FP8_ERR_ALIGN;
+  return linear_fwd_impl(X, N, K, cache, h, recipe, Y, ctx, ws, ws_bytes, stream,
+                         static_cast<const float *>(x_partials));
+}
+
+fp8_status fp8_linear_bwd_after_amax(const void *dY, const void *dy_partials, int64_t N, int64_t O,
+                                     const void *ctx, fp8_weight_cache *cache, fp8_weight_handle h,
+                                     fp8_recipe recipe, void *dX, void *dW, void *ws,
+                                     size_t ws_bytes, fp8_stream_t stream) {
+  if (!dy_partials && N > 0) return FP8_ERR_INVALID_ARG;
+  if (dy_partials && !aligned16(dy_partials)) return FP8_ERR_ALIGN;
+  return linear_bwd_impl(dY, N, O, ctx, cache, h, recipe, dX, dW, ws, ws_bytes, stream,
+                         static_cast<const float *>(dy_partials));
 }
 
 // ---------------------------------------------------------------- fused producers

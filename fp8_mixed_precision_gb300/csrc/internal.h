@@ -33,10 +33,15 @@ int num_sms();
 int tensorwise_partials_count(int64_t rows, int64_t cols);
 
 // mode: 0 tensorwise, 1 1x128 blocks, 2 128x128 tiles; fmt: fp8_format.
+// Tensorwise with amax_done: the first pass already wrote `partials`
+// (launch_amax_partials on the same tensor); only the cast runs.
 cudaError_t launch_quantize(const void *x, int64_t rows, int64_t cols, int mode, int fmt,
                             uint8_t *out_row, uint8_t *out_col, float *row_scale,
                             float *row_scale_inv, float *col_scale, float *col_scale_inv,
-                            float *partials, cudaStream_t st);
+                            float *partials, cudaStream_t st, bool amax_done = false);
+// Tensorwise first pass alone: tensorwise_partials_count(rows, cols) partial maxima.
+cudaError_t launch_amax_partials(const void *x, int64_t rows, int64_t cols, float *partials,
+                                 cudaStream_t st);
 
 // Delayed scaling: cast with the scale of the history's maximum, then write
 // this tensor's amax to hist[step % hist_len] (partials: >= 2 x SMs floats).

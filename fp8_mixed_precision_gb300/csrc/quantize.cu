@@ -560,10 +560,19 @@ static cudaError_t launch_tile(const QParams &p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_amax_partials(const void *x, int64_t rows, int64_t cols, float *partials,
+                                 cudaStream_t st) {
+  const int g = tensorwise_partials_count(rows, cols);
+  LaunchScope ls("quant_amax_tensorwise", st, 2.0 * rows * cols, 0.0);
+  amax_partials_kernel<<<g, kAmaxThreads, 0, st>>>(static_cast<const uint4 *>(x), rows * cols / 8,
+                                                   partials);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quantize(const void *x, int64_t rows, int64_t cols, int mode, int fmt,
                             uint8_t *out_row, uint8_t *out_col, float *row_scale,
                             float *row_scale_inv, float *col_scale, float *col_scale_inv,
-                            float *partials, cudaStream_t st) {
+                            float *partials, cudaStream_t st, bool amax_done) {
   QParams p;
   p.x = static_cast<const uint16_t *>(x);
   p.x2 = nullptr;
@@ -581,15 +590,11 @@ cudaError_t launch_quantize(const void *x, int64_t rows, int64_t cols, int mode,
   p.hist_len = 0;
   p.cur_partials = nullptr;
   if (mode == Q_TENSOR) {
-    const int g = tensorwise_partials_count(rows, cols);
-    {
-      LaunchScope ls("quant_amax_tensorwise", st, 2.0 * rows * cols, 0.0);
-      amax_partials_kernel<<<g, kAmaxThreads, 0, st>>>(static_cast<const uint4 *>(x),
-                                                       rows * cols / 8, partials);
+    if (!amax_done) {
+      cudaError_t e = launch_amax_partials(x, rows, cols, partials, st);
+      if (e != cudaSuccess) return e;
     }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    p.n_partials = g;
+    p.n_partials = tensorwise_partials_count(rows, cols);
     return fmt == FP8_FORMAT_E4M3 ? launch_tile<Q_TENSOR, FP8_FORMAT_E4M3>(p, st)
                                   : launch_tile<Q_TENSOR, FP8_FORMAT_E5M2>(p, st);
   }

@@ -245,6 +245,35 @@ fp8_status fp8_linear_bwd(const void *dY, int64_t N, int64_t O, const void *ctx,
                           fp8_weight_cache *cache, fp8_weight_handle h, fp8_recipe recipe,
                           void *dX, void *dW, void *ws, size_t ws_bytes, fp8_stream_t stream);
 
+/* ------------------------------------------------------------------ split tensorwise passes
+ * Current tensorwise scaling is two passes over a tensor: per-CTA maxima of
+ * |x|, then the cast with scale = fmax / (maximum of those partials).  The
+ * first pass reads the whole tensor and nothing else, and its CTAs need almost
+ * no shared memory, so it can run on another stream beside a GEMM or a cast
+ * on the same GPU.
+ *   fp8_amax_partials: the first pass alone over bf16 x [rows, cols], into
+ *     `partials` (device, fp8_quantize_workspace_size(TENSORWISE, rows, cols)
+ *     bytes, 16-byte aligned).
+ *   fp8_linear_fwd_after_amax / fp8_linear_bwd_after_amax: fp8_linear_fwd /
+ *     fp8_linear_bwd whose X (resp. dY) quantization runs only the cast,
+ *     reading partials that fp8_amax_partials wrote for that same tensor.
+ *     The caller orders the two (e.g. an event between the streams).
+ *     Tensorwise and delayed recipes (their activations use current
+ *     tensorwise scaling); the block recipe returns FP8_ERR_UNSUPPORTED.
+ * Results are bit for bit those of fp8_linear_fwd / fp8_linear_bwd.
+ * Errors: as fp8_linear_fwd / bwd and fp8_quantize (WORKSPACE for a short
+ * partials buffer). */
+fp8_status fp8_amax_partials(const void *x, int64_t rows, int64_t cols, void *partials,
+                             size_t partials_bytes, fp8_stream_t stream);
+fp8_status fp8_linear_fwd_after_amax(const void *X, const void *x_partials, int64_t N, int64_t K,
+                                     fp8_weight_cache *cache, fp8_weight_handle h,
+                                     fp8_recipe recipe, void *Y, void *ctx, void *ws,
+                                     size_t ws_bytes, fp8_stream_t stream);
+fp8_status fp8_linear_bwd_after_amax(const void *dY, const void *dy_partials, int64_t N, int64_t O,
+                                     const void *ctx, fp8_weight_cache *cache, fp8_weight_handle h,
+                                     fp8_recipe recipe, void *dX, void *dW, void *ws,
+                                     size_t ws_bytes, fp8_stream_t stream);
+
 /* ------------------------------------------------------------------ fused producers
  * Quantization fused into the producer of the quantized tensor (block recipe
  * only; other recipes return FP8_ERR_UNSUPPORTED).  The bf16 intermediate is

@@ -175,3 +175,62 @@ def test_fused_equals_plain_fp8(fp, recipe):
     torch.cuda.synchronize()
     for a, b, name in ((y, y2, "Y"), (dx, dx2, "dX"), (dw, dw2, "dW")):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16)), name
+
+
+@pytest.mark.parametrize("recipe", ["tensorwise", "delayed"])
+def test_split_amax_pass_equals_one_call(fp, recipe):
+    """fp8_amax_partials on a second stream, then the *_after_amax linear calls
+    on the first: bit for bit the results of fp8_linear_fwd / fp8_linear_bwd."""
+    N, K, O = 2048, 512, 1024
+    x, w, dy = syn.linear_inputs(N, K, O, device="cuda")
+    outs = {}
+    for split in (False, True):
+        cache = fp.WeightCache()
+        h = cache.register(w, recipe)
+        cache.begin_cycle()
+        cache.get(h, 0, True)
+        ws = fp.linear_workspace(recipe, N, K, O, "cuda")
+        ctx = fp.LinearContext(fp._empty_bytes(fp._ctx_bytes(recipe, N, K), "cuda"), N, K)
+        y = torch.empty((N, O), dtype=torch.bfloat16, device="cuda")
+        dx = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+        dw = torch.empty((O, K), dtype=torch.bfloat16, device="cuda")
+        if split:
+            aux = torch.cuda.Stream()
+            aux.wait_stream(torch.cuda.current_stream())
+            px, pdy = fp.amax_partials_buffer(N, K, "cuda"), fp.amax_partials_buffer(N, O, "cuda")
+            ex, ed = torch.cuda.Event(), torch.cuda.Event()
+            with torch.cuda.stream(aux):
+                fp.fp8_amax_partials(x, px)
+                ex.record(aux)
+                fp.fp8_amax_partials(dy, pdy)
+                ed.record(aux)
+            torch.cuda.current_stream().wait_event(ex)
+            fp.fp8_linear_fwd_after_amax(x, px, cache, h, recipe, ws, y, ctx)
+            torch.cuda.current_stream().wait_event(ed)
+            fp.fp8_linear_bwd_after_amax(dy, pdy, ctx, cache, h, recipe, ws, dx, dw)
+        else:
+            fp.fp8_linear_fwd(x, cache, h, recipe, ws=ws, y=y, ctx=ctx)
+            fp.fp8_linear_bwd(dy, ctx, cache, h, recipe, ws=ws, dx=dx, dw=dw)
+        torch.cuda.synchronize()
+        outs[split] = (y, dx, dw)
+    assert fp.fp8_get_device_status() == 0
+    for a, b, name in zip(outs[False], outs[True], ("Y", "dX", "dW")):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), name
+
+
+def test_split_amax_pass_refuses_block_recipe(fp):
+    N, K, O = 256, 256, 256
+    x, w, dy = syn.linear_inputs(N, K, O, device="cuda")
+    cache = fp.WeightCache()
+    h = cache.register(w, "block")
+    cache.begin_cycle()
+    cache.get(h, 0, True)
+    ws = fp.linear_workspace("block", N, K, O, "cuda")
+    ctx = fp.LinearContext(fp._empty_bytes(fp._ctx_bytes("block", N, K), "cuda"), N, K)
+    px = fp.amax_partials_buffer(N, K, "cuda")
+    y = torch.empty((N, O), dtype=torch.bfloat16, device="cuda")
+    n0 = fp.fp8_launch_count()
+    with pytest.raises(fp.FP8Error) as e:
+        fp.fp8_linear_fwd_after_amax(x, px, cache, h, "block", ws, y, ctx)
+    assert e.value.status == 7
+    assert fp.fp8_launch_count() == n0
