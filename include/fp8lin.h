@@ -253,7 +253,7 @@ fp8_status fp8_linear_bwd(const void *dY, int64_t N, int64_t O, const void *ctx,
  * on the same GPU.
  *   fp8_amax_partials: the first pass alone over bf16 x [rows, cols], into
  *     `partials` (device, fp8_quantize_workspace_size(TENSORWISE, rows, cols)
- *     bytes, 16-byte aligned).
+ *     bytes, 16-byte aligned; the contents are the library's own format).
  *   fp8_linear_fwd_after_amax / fp8_linear_bwd_after_amax: fp8_linear_fwd /
  *     fp8_linear_bwd whose X (resp. dY) quantization runs only the cast,
  *     reading partials that fp8_amax_partials wrote for that same tensor.
