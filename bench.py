@@ -247,6 +247,15 @@ def run_ours(args):
                                          L["dw"])
 
     step = step_overlap if args.schedule == "overlap" else step_serial
+    # the first call, cold (per-device kernel attributes and occupancy queries,
+    # first touch of every buffer), reported on its own
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    f0.record(stream)
+    step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    first_ms = f0.elapsed_time(f1)
     for _ in range(args.warmup):        # both schedules, so either can be timed warm
         step_overlap()
         step_serial()
@@ -264,14 +273,25 @@ def run_ours(args):
         barrier(world)
         torch.cuda.synchronize()
         n_launch0 = fp.fp8_launch_count()
+        # the K steps in up to 5 groups, an event at each boundary (5 events in
+        # all): the spread of the group means is reported with the total
+        ngroups = min(5, args.steps)
+        bounds = [args.steps * gi // ngroups for gi in range(ngroups + 1)]
+        gev = [torch.cuda.Event(enable_timing=True) for _ in range(ngroups - 1)]
         t0.record(stream)
-        for _ in range(args.steps):
-            step()
+        for gi in range(ngroups):
+            for _ in range(bounds[gi + 1] - bounds[gi]):
+                step()
+            if gi < ngroups - 1:
+                gev[gi].record(stream)
         t1.record(stream)
         torch.cuda.synchronize()
         barrier(world)
         n_launch = fp.fp8_launch_count() - n_launch0
     clocks = clk.summary()
+    marks = [t0] + gev + [t1]
+    group_ms = [marks[gi].elapsed_time(marks[gi + 1]) / (bounds[gi + 1] - bounds[gi])
+                for gi in range(ngroups)]
     p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     fp.fp8_profile_begin()
@@ -372,6 +392,9 @@ def run_ours(args):
             "other_schedule_ms_per_step": {("serial" if args.schedule == "overlap"
                                             else "overlap"): other_ms_step},
             "profiled_ms_per_step": profiled_ms_step,
+            "step_ms_groups": {"median": statistics.median(group_ms), "min": min(group_ms),
+                               "max": max(group_ms), "groups": group_ms},
+            "first_call_ms": first_ms,
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
