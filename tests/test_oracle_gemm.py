@@ -209,3 +209,33 @@ def test_grad_accumulate_fp32():
     assert list(acc) == [2.0, 2.0, -2.0, 0.0]
     big = np.array([2.0 ** 24], np.float32)
     assert o.grad_accumulate(big, np.array([0x3F80], np.uint16))[0] == 2.0 ** 24   # fp32 RNE tie-to-even
+
+
+def test_mlp_gelu_stage_by_central_differences():
+    # In the MLP backward, dH = dA * GELU'(H) with H the bf16 fc1 output and
+    # dA the fc2 dgrad output.  Check that wiring (H, not A; dA, not dY) with a
+    # central difference of the fp64 GELU, independent of gelu_grad_f64.
+    N, d, ffn = 256, 128, 256
+    x = syn.bits(syn.bf16_normal((N, d), 1.0, 61))
+    w1 = syn.bits(syn.bf16_normal((ffn, d), 0.02, 62))
+    w2 = syn.bits(syn.bf16_normal((d, ffn), 0.02, 63))
+    dy = syn.bits(syn.bf16_normal((N, d), 1e-3, 64))
+    r = o.mlp_fwd_bwd(x, w1, w2, dy, "block")
+    h = o.bf16_to_f32(r["h"]).astype(np.float64)
+    da = o.bf16_to_f32(r["da"]).astype(np.float64)
+    dh = o.bf16_to_f32(r["dh"]).astype(np.float64)
+    rng = np.random.default_rng(7)
+    for _ in range(64):
+        i, j = int(rng.integers(N)), int(rng.integers(ffn))
+        hv = h[i, j]
+        eps = 1e-5 * max(1.0, abs(hv))
+        slope = (o.gelu_f64(np.array([hv + eps])) - o.gelu_f64(np.array([hv - eps])))[0] / (2 * eps)
+        want = da[i, j] * slope
+        # dH is rounded once to bf16: within one bf16 ulp of the product (plus
+        # the difference quotient's own error)
+        assert abs(dh[i, j] - want) <= 2.0 ** -8 * abs(want) + 1e-12 * abs(da[i, j]) + 1e-30, \
+            (i, j, dh[i, j], want)
+    # the forward stage: A = bf16(GELU(H)) from the same H
+    a = o.bf16_to_f32(r["a"]).astype(np.float64)
+    ref = o.gelu_f64(h)
+    assert np.all(np.abs(a - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-30)
