@@ -68,10 +68,14 @@ static_assert(sizeof(SmemCtl) <= 12288, "control block");
 // barriers and flags only (the column-scale area serves 1x128 x 1x128 alone)
 constexpr int kCtlSmall = (int)((offsetof(SmemCtl, bscale) + 127) / 128 * 128);
 
-// MH = M halves per tile.  MH = 2 gives 256 x BN tiles made of two M = 128
-// MMAs sharing each B stage: for BN = 256, 1.5x fewer operand bytes per flop
-// enter the SM.  The two accumulators fill TMEM, so a tile's epilogue does not
-// overlap the next tile's MMAs: used for deep-K tensor-scaled GEMMs only.
+// Per-CTA configuration.
+//   MH  M halves per tile: MH = 2 gives 256 x BN tiles made of two M = 128
+//       MMAs sharing each B stage (for BN = 256, 1.5x fewer operand bytes per
+//       flop enter the SM); the two accumulators fill TMEM, so a tile's
+//       epilogue does not overlap the next tile's MMAs (deep-K tensor-scaled
+//       GEMMs only).
+//   PR  CTA pair (cluster of 2, cta_group::2 MMAs): each CTA stages its own
+//       A rows and half of the B tile.
 // Shared memory: operand ring, bf16 output staging (none for split-K, which
 // writes fp32 partials from registers) and the control block (the column
 // scale area only for 1x128 x 1x128).
