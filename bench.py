@@ -263,6 +263,29 @@ def run_ours(args):
     st = fp.fp8_get_device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} after warm-up")
+    launches_per_step = fp.fp8_launch_count()
+    step()
+    torch.cuda.synchronize()
+    launches_per_step = fp.fp8_launch_count() - launches_per_step
+
+    # One step captured in a CUDA graph: every replay runs the same kernels
+    # with the same arguments (the weights are re-quantized each replay, as in
+    # the eager step), without the host's per-launch work between them.
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()                          # warm the capture stream
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize()
+    eager_step = step
+    timed_step = graph.replay if args.launch == "graph" else eager_step
+    for _ in range(args.warmup):
+        timed_step()
+    torch.cuda.synchronize()
 
     # ---- device-resident timing: `value` comes from K steps with no per-kernel
     # events (recording two events around every launch costs a few percent of
@@ -281,13 +304,15 @@ def run_ours(args):
         t0.record(stream)
         for gi in range(ngroups):
             for _ in range(bounds[gi + 1] - bounds[gi]):
-                step()
+                timed_step()
             if gi < ngroups - 1:
                 gev[gi].record(stream)
         t1.record(stream)
         torch.cuda.synchronize()
         barrier(world)
         n_launch = fp.fp8_launch_count() - n_launch0
+        if args.launch == "graph":      # replays launch the captured kernels
+            n_launch = launches_per_step * args.steps
     clocks = clk.summary()
     marks = [t0] + gev + [t1]
     group_ms = [marks[gi].elapsed_time(marks[gi + 1]) / (bounds[gi + 1] - bounds[gi])
@@ -297,7 +322,7 @@ def run_ours(args):
     fp.fp8_profile_begin()
     p0.record(stream)
     for _ in range(args.steps):
-        step()
+        eager_step()
     p1.record(stream)
     torch.cuda.synchronize()
     kstats = fp.fp8_profile_end()
@@ -312,6 +337,17 @@ def run_ours(args):
     o1.record(stream)
     torch.cuda.synchronize()
     other_ms_step = reduce_max(o0.elapsed_time(o1), world, dev) / args.steps
+    # the other launch mode, for reference
+    other_launch = eager_step if args.launch == "graph" else graph.replay
+    q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    q0.record(stream)
+    for _ in range(args.steps):
+        other_launch()
+    q1.record(stream)
+    torch.cuda.synchronize()
+    other_launch_ms = reduce_max(q0.elapsed_time(q1), world, dev) / args.steps
+    del graph
     ms_local = t0.elapsed_time(t1)
     ms_total = reduce_max(ms_local, world, dev)
     ms_step = ms_total / args.steps
@@ -388,10 +424,14 @@ def run_ours(args):
                        "parallelism": f"dp{world} (replicas, no collective)",
                        "schedule": ("tensorwise amax passes on a second stream beside the "
                                     "GEMMs and casts" if args.schedule == "overlap"
-                                    else "one stream")},
+                                    else "one stream"),
+                       "launch": ("one step captured as a CUDA graph, replayed"
+                                  if args.launch == "graph" else "eager launches")},
             "other_schedule_ms_per_step": {("serial" if args.schedule == "overlap"
                                             else "overlap"): other_ms_step},
             "profiled_ms_per_step": profiled_ms_step,
+            "other_launch_ms_per_step": {("eager" if args.launch == "graph" else "graph"):
+                                         other_launch_ms},
             "step_ms_groups": {"median": statistics.median(group_ms), "min": min(group_ms),
                                "max": max(group_ms), "groups": group_ms},
             "first_call_ms": first_ms,
@@ -774,6 +814,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--launch", choices=["graph", "eager"], default="graph",
+                    help="graph (default): time replays of one step captured as a CUDA graph; "
+                         "eager: one library call per linear per step")
     ap.add_argument("--schedule", choices=["serial", "overlap"], default="serial",
                     help="overlap: tensorwise amax passes on a second stream")
     ap.add_argument("--no-mlp", action="store_true",
