@@ -22,6 +22,7 @@
 //   warps 2-9   epilogue: tcgen05.ld from TMEM, scale, round to bf16, stage
 //               32x64 slabs in 128B-swizzled shared memory, TMA bulk stores.
 //               Warp w reads TMEM lanes 32*(w%4)..+31 and column half (w-2)/4.
+//               (1x128 x 1x128: warps 2-17, column quarter (w-2)/4.)
 // TMEM holds 512/BN accumulator buffers used round-robin, so the epilogue of
 // one tile (tensor scaling) or one K block (block scaling) overlaps the
 // following MMAs.  Deep-K tensor-scaled GEMMs use 256-row tiles (two M
@@ -44,12 +45,7 @@ namespace fp8lin {
 namespace {
 
 constexpr int BM = 128, BK = 128;
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 512;
-// bf16 output staging: per epilogue warp Cfg::kOutSlabs 32-row x 64-column
-// slabs (32 x 128 bytes, 128-byte swizzled) feeding TMA bulk-tensor stores.
-constexpr int kOutSlabBytes = 32 * 128;
 constexpr int kSmemBudget = 227 * 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s
@@ -62,9 +58,13 @@ struct SmemCtl {
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
-  float bscale[kEpiWarps][256];  // 1x128 x 1x128: column scales of 4 K blocks x 64 columns
+  // 1x128 x 1x128 only: per epilogue warp, the column and row scales of the
+  // current group of 4 K blocks as [K block][column] and [K block][row], and
+  // the cp.async staging slots of the next group's column and row scales
+  float bscale[4096];
+  float4 sstage[1024];
 };
-static_assert(sizeof(SmemCtl) <= 12288, "control block");
+constexpr int kCtlFull = (int)((sizeof(SmemCtl) + 127) / 128 * 128);
 // barriers and flags only (the column-scale area serves 1x128 x 1x128 alone)
 constexpr int kCtlSmall = (int)((offsetof(SmemCtl, bscale) + 127) / 128 * 128);
 
@@ -76,24 +76,38 @@ constexpr int kCtlSmall = (int)((offsetof(SmemCtl, bscale) + 127) / 128 * 128);
 //       GEMMs only).
 //   PR  CTA pair (cluster of 2, cta_group::2 MMAs): each CTA stages its own
 //       A rows and half of the B tile.
+// Epilogue warps: 8 (two per TMEM lane quarter, each taking half of the
+// tile's columns), or 16 for the 1x128 x 1x128 promotion (four per lane
+// quarter, 32 columns each), whose per-K-block TMEM drain is latency-bound
+// and needs more warps per scheduler to overlap it.
 // Shared memory: operand ring, bf16 output staging (none for split-K, which
 // writes fp32 partials from registers) and the control block (the column
-// scale area only for 1x128 x 1x128).
+// scale area only for 1x128 x 1x128).  Output slabs are 32 rows x 64 columns
+// (128 bytes per row, 128-byte swizzle) for 64-column warps and 32 x 32
+// (64 bytes per row, unswizzled) for 32-column warps.
 template <int SCALING, bool SPLIT, int BN, int MH = 1, bool PR = false>
 struct Cfg {
+  static constexpr int kEpi = SCALING == FP8_SCALING_1x128_1x128 ? 16 : 8;  // epilogue warps
+  static constexpr int kThreads = 64 + 32 * kEpi;
+  static constexpr int kCols = BN * 4 / kEpi;  // tile columns per epilogue warp
   static constexpr int kStageA = MH * BM * BK;  // bytes
   static constexpr int kStageB = (PR ? BN / 2 : BN) * BK;  // a pair CTA holds half of B
   static constexpr int kStageBytes = kStageA + kStageB;
   static constexpr int kAccBufs = (int)kTmemCols / BN;
-  static constexpr int kCtlBytes = SCALING == FP8_SCALING_1x128_1x128 ? 12288 : kCtlSmall;
-  static constexpr int kOutSlabs = SPLIT ? 0 : (MH == 2 ? 1 : 2);
-  static constexpr int kOutBytes = kEpiWarps * kOutSlabs * kOutSlabBytes;
+  static constexpr int kCtlBytes = SCALING == FP8_SCALING_1x128_1x128 ? kCtlFull : kCtlSmall;
+  static constexpr int kOutSlabBytes = kCols == 32 ? 32 * 64 : 32 * 128;
+  static constexpr int kOutSlabs = SPLIT ? 0 : (MH == 2 || kCols == 32 ? 1 : 2);
+  static constexpr int kOutBytes = kEpi * kOutSlabs * kOutSlabBytes;
   static constexpr int kRing = kSmemBudget - 1024 - kOutBytes - kCtlBytes;
   static constexpr int kStages = kRing / kStageBytes < kMaxStages ? kRing / kStageBytes : kMaxStages;
   static constexpr size_t kSmemBytes =
       1024 + (size_t)kStages * kStageBytes + (size_t)kOutBytes + kCtlBytes;
   static_assert(kStages >= 2, "shared memory too small for the operand ring");
   static_assert(MH == 1 || (MH == 2 && kAccBufs == 2), "two M halves fill TMEM exactly");
+  static_assert(kCols == 32 || kCols % 64 == 0, "epilogue column split");
+  static_assert(SCALING != FP8_SCALING_1x128_1x128 || (kCols == 32 && kEpi * 256 <= 4096 &&
+                                                        kEpi * 64 <= 1024),
+                "scale staging areas");
 };
 
 __device__ unsigned g_gemm_status;
@@ -216,7 +230,7 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
 }
 
 template <int SCALING, bool SPLIT, int BN, int MH, bool PR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<SCALING, SPLIT, BN, MH, PR>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const GemmArgs g) {
   using C = Cfg<SCALING, SPLIT, BN, MH, PR>;
@@ -237,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint16_t kBoth = 0x3;
   constexpr int kStages = C::kStages;
   constexpr int NB = C::kAccBufs;
-  constexpr int kHalf = BN / 2;           // columns per epilogue warp
+  constexpr int kHalf = C::kCols;         // columns per epilogue warp
   constexpr int kSlabs = kHalf / 64;      // 64-column slabs per epilogue warp per tile
   // block scaling: the partial is consumed in kCw-column TMEM loads (16 for
   // 256-wide tiles, which keep 128 fp32 accumulators per thread in registers)
@@ -247,8 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kPre = BN == 256 ? 2 : 4; // K blocks of scales held ahead in registers
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned base, by pointer arithmetic on the shared array (so the
+  // compiler keeps every derived pointer in the shared window)
+  uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t *out_stage = smem + (size_t)kStages * C::kStageBytes;
   SmemCtl *ctl = reinterpret_cast<SmemCtl *>(out_stage + C::kOutBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -260,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < NB; ++b) {
       ptx::mbar_init(&ctl->acc_full[b], 1);
-      ptx::mbar_init(&ctl->acc_empty[b], PR ? 2 * kEpiWarps : kEpiWarps);
+      ptx::mbar_init(&ctl->acc_empty[b], PR ? 2 * C::kEpi : C::kEpi);
     }
     ptx::mbar_init(&ctl->mma_done, 1);
     ctl->abort = 0;
@@ -395,12 +410,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;          // TMEM lane quarter this warp may access
-    const int h = (warp - 2) >> 2;   // column half of the tile
+    const int h = (warp - 2) >> 2;   // column group of the tile (kHalf columns)
     const int r = q * 32 + lane;     // tile row owned by this thread
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * kHalf);
     uint32_t nacc = 0;
     uint32_t nout = 0;  // bf16 slabs this warp has handed to TMA stores
-    uint8_t *slabs = out_stage + (size_t)(warp - 2) * C::kOutSlabs * kOutSlabBytes;
+    uint8_t *slabs = out_stage + (size_t)(warp - 2) * C::kOutSlabs * C::kOutSlabBytes;
     float s_tensor = 0.0f;
     if (SCALING == FP8_SCALING_TENSOR) s_tensor = __fmul_rn(g.a_sinv[0], g.b_sinv[0]);
     // TMEM buffer ab drained by this warp: tell the MMA issuer (the leader's
@@ -421,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         store32_f32(g, split, slab_y + lane, col0 + 32, v1, scale);
       } else {
         if (slab_y >= g.M || col0 >= g.N) return;  // slab entirely outside C
-        uint8_t *slab = slabs + (nout % C::kOutSlabs) * kOutSlabBytes;
+        uint8_t *slab = slabs + (nout % C::kOutSlabs) * C::kOutSlabBytes;
         // the store kOutSlabs slabs ago has finished reading this buffer
         if (lane == 0) ptx::bulk_wait_read<C::kOutSlabs - 1>();
         __syncwarp();
@@ -485,73 +500,97 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the loads are issued kPre blocks before their use, hiding their latency.
         bool ok = true;
         if constexpr (SCALING == FP8_SCALING_1x128_1x128) {
-          // Scales move in groups of 4 K blocks: one 16-byte load per row (A)
-          // and per column (B) fetches a group; the column scales of the
-          // current group are staged in this warp's shared slice once.
-          auto ld4 = [&](const float *row, int k) -> float4 {
-            if (g.vec4 && k + 3 < kb1) return *reinterpret_cast<const float4 *>(row + k);
-            float4 r;
-            r.x = k < kb1 ? row[k] : 0.0f;
-            r.y = k + 1 < kb1 ? row[k + 1] : 0.0f;
-            r.z = k + 2 < kb1 ? row[k + 2] : 0.0f;
-            r.w = k + 3 < kb1 ? row[k + 3] : 0.0f;
-            return r;
+          // Every element's scale is (row scale) x (column scale) of its K
+          // block.  The partial is read with the 16x256b TMEM shape: thread
+          // (rr, cc) = (lane / 4, lane % 4) holds rows rr + 8i (i = 0..3) of
+          // the warp's 32-row quarter and columns 8j + 2cc, +1 (j = 0..3) of
+          // its 32 columns, so it needs 8 column scales and 4 row scales per
+          // K block instead of 32 column scales (32x32b shape) - fewer bytes
+          // through the shared-memory / TMEM load path into registers, which
+          // bounds this promotion.  acc[4i + j] holds the pair (row i, pair j).
+          static_assert(kHalf == 32, "16x256b promotion: 32 columns per warp");
+          const int rr = lane >> 2, cc = lane & 3;
+          const int64_t n_st = colbase + lane;  // column whose scales this lane stages
+          const bool nok = n_st < g.N;
+          const float *brow = g.b_sinv + (nok ? n_st : g.N - 1) * g.lds_b;
+          // per warp: current group as [K block][32 columns] and [K block][32 rows]
+          float *bsw = ctl->bscale + (warp - 2) * 256;
+          float *asw = bsw + 128;
+          // cp.async staging, one group ahead: [lane] column scales, then [lane] row scales
+          float4 *stg = ctl->sstage + (warp - 2) * 64;
+          // Scales move in groups of 4 K blocks; each lane copies the 4 scales
+          // of its staging column and of row q*32 + lane with cp.async
+          // (nothing held in registers while in flight).
+          auto fetch4 = [&](float4 *dst, const float *row, int k) {
+            if (g.vec4 && k + 3 < kb1) {
+              ptx::cp_async16(dst, row + k);
+            } else {
+              float *d = reinterpret_cast<float *>(dst);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)  // past kb1: zero fill from a valid address
+                ptx::cp_async4(d + i, row + (k + i < kb1 ? k + i : kb0), k + i < kb1 ? 4u : 0u);
+            }
           };
-          const int64_t n0 = colbase + lane, n1 = colbase + 32 + lane;
-          const bool n0ok = n0 < g.N, n1ok = n1 < g.N;
-          const float *brow0 = g.b_sinv + (n0ok ? n0 : g.N - 1) * g.lds_b;
-          const float *brow1 = g.b_sinv + (n1ok ? n1 : g.N - 1) * g.lds_b;
-          float *bsw = ctl->bscale[warp - 2];
-          float4 a_cur = ld4(arow, kb0), b0_cur = ld4(brow0, kb0), b1_cur = ld4(brow1, kb0);
+          auto fetch = [&](int k) {
+            fetch4(stg + lane, brow, k);
+            fetch4(stg + 32 + lane, arow, k);
+            ptx::cp_async_commit();
+          };
+          fetch(kb0);
           for (int g0 = kb0; ok && g0 < kb1; g0 += 4) {
-            const float4 a_nxt = ld4(arow, g0 + 4), b0_nxt = ld4(brow0, g0 + 4),
-                         b1_nxt = ld4(brow1, g0 + 4);
-            __syncwarp();
-            bsw[0 * 64 + lane] = n0ok ? b0_cur.x : 0.0f;
-            bsw[1 * 64 + lane] = n0ok ? b0_cur.y : 0.0f;
-            bsw[2 * 64 + lane] = n0ok ? b0_cur.z : 0.0f;
-            bsw[3 * 64 + lane] = n0ok ? b0_cur.w : 0.0f;
-            bsw[0 * 64 + 32 + lane] = n1ok ? b1_cur.x : 0.0f;
-            bsw[1 * 64 + 32 + lane] = n1ok ? b1_cur.y : 0.0f;
-            bsw[2 * 64 + 32 + lane] = n1ok ? b1_cur.z : 0.0f;
-            bsw[3 * 64 + 32 + lane] = n1ok ? b1_cur.w : 0.0f;
+            ptx::cp_async_wait_all();
+            const float4 bv = stg[lane], av = stg[32 + lane];  // this lane's own slots
+            if (g0 + 4 < kb1) fetch(g0 + 4);
+            __syncwarp();  // the previous group's reads of bsw / asw are done
+            bsw[0 * 32 + lane] = nok ? bv.x : 0.0f;
+            bsw[1 * 32 + lane] = nok ? bv.y : 0.0f;
+            bsw[2 * 32 + lane] = nok ? bv.z : 0.0f;
+            bsw[3 * 32 + lane] = nok ? bv.w : 0.0f;
+            asw[0 * 32 + lane] = av.x;
+            asw[1 * 32 + lane] = av.y;
+            asw[2 * 32 + lane] = av.z;
+            asw[3 * 32 + lane] = av.w;
             __syncwarp();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               if (g0 + kk >= kb1) break;
               const uint32_t ab = nacc % NB, aph = (nacc / NB) & 1;
-              const float sa = kk == 0 ? a_cur.x : kk == 1 ? a_cur.y : kk == 2 ? a_cur.z : a_cur.w;
               if (!wait_bar<PR>(&ctl->acc_full[ab], aph, abort)) { ok = false; break; }
               ptx::tc_fence_after();
-              const uint64_t sa2 = pk(sa, sa);
-              const float4 *bq = reinterpret_cast<const float4 *>(bsw + kk * 64);
+              uint64_t sb[4];  // column-scale pairs of this thread's 4 column pairs
 #pragma unroll
-              for (int c = 0; c < 2; ++c) {  // two 32-column TMEM chunks
-                uint32_t raw[32];
-                ptx::tmem_ld32(tl + ab * BN + 32 * c, raw);
+              for (int j = 0; j < 4; ++j) {
+                const float2 b2 = *reinterpret_cast<const float2 *>(bsw + kk * 32 + 8 * j + 2 * cc);
+                sb[j] = pk(b2.x, b2.y);
+              }
+#pragma unroll
+              for (int hb = 0; hb < 2; ++hb) {  // TMEM lanes q*32 + 16 hb .. +15
+                uint32_t raw[16];
+                ptx::tmem_ld16x256b_x4(tl + ((uint32_t)(16 * hb) << 16) + ab * BN, raw);
                 ptx::tmem_ld_wait();
-                if (c == 1) {  // the partial is in registers: free the TMEM buffer
+                if (hb == 1) {  // the partial is in registers: free the TMEM buffer
                   ptx::tc_fence_before();
                   __syncwarp();
                   if (lane == 0) release_acc(ab);
                 }
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const float4 b4 = bq[8 * c + j];  // scales of columns 32c + 4j .. +3
-                  const uint64_t s0 = mul2(sa2, pk(b4.x, b4.y)), s1 = mul2(sa2, pk(b4.z, b4.w));
-                  const int p = 16 * c + 2 * j;
-                  acc[p] = fma2(pk(__uint_as_float(raw[4 * j]), __uint_as_float(raw[4 * j + 1])), s0,
-                                acc[p]);
-                  acc[p + 1] = fma2(pk(__uint_as_float(raw[4 * j + 2]), __uint_as_float(raw[4 * j + 3])),
-                                    s1, acc[p + 1]);
+                for (int ii = 0; ii < 2; ++ii) {
+                  const int i = 2 * hb + ii;  // row rr + 8i
+                  const float sa = asw[kk * 32 + rr + 8 * i];
+                  const uint64_t sa2 = pk(sa, sa);
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    const uint64_t sc = mul2(sa2, sb[j]);
+                    acc[4 * i + j] = fma2(pk(__uint_as_float(raw[4 * j + 2 * ii]),
+                                             __uint_as_float(raw[4 * j + 2 * ii + 1])),
+                                          sc, acc[4 * i + j]);
+                  }
                 }
               }
               ++nacc;
             }
-            a_cur = a_nxt;
-            b0_cur = b0_nxt;
-            b1_cur = b1_nxt;
           }
+          ptx::cp_async_wait_all();  // no scale copy in flight past the tile (abort path)
         } else {
         float ra[kPre], rb[kPre][kBl];
         auto load_scales = [&](int k, float &a, float (&b)[kBl]) {
@@ -594,15 +633,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         }
         if (!ok) break;
+        if constexpr (SCALING == FP8_SCALING_1x128_1x128) {
+          // rows slab_y + rr + 8i, columns colbase + 8j + 2cc and +1
+          const int rr = lane >> 2, cc = lane & 3;
+          if constexpr (SPLIT) {
 #pragma unroll
-        for (int s = 0; s < kSlabs; ++s) {
-          float v0[32], v1[32];
+            for (int i = 0; i < 4; ++i) {
+              const int64_t mm = slab_y + rr + 8 * i;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            upk(acc[32 * s + j], v0[2 * j], v0[2 * j + 1]);
-            upk(acc[32 * s + 16 + j], v1[2 * j], v1[2 * j + 1]);
+              for (int j = 0; j < 4; ++j) {
+                const int64_t n = colbase + 8 * j + 2 * cc;  // N is even: n < N covers n + 1
+                if (mm >= g.M || n >= g.N) continue;
+                float2 v;
+                upk(acc[4 * i + j], v.x, v.y);
+                *reinterpret_cast<float2 *>(static_cast<float *>(g.out) +
+                                            ((int64_t)split * g.M + mm) * g.N + n) = v;
+              }
+            }
+          } else if (slab_y < g.M && colbase < g.N) {
+            // one 32 x 32 bf16 slab (64-byte rows, unswizzled), staged once per tile
+            uint8_t *slab = slabs + (nout % C::kOutSlabs) * C::kOutSlabBytes;
+            if (lane == 0) ptx::bulk_wait_read<C::kOutSlabs - 1>();
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                float x, y;
+                upk(acc[4 * i + j], x, y);
+                __nv_bfloat162 b = __floats2bfloat162_rn(x, y);
+                *reinterpret_cast<__nv_bfloat162 *>(slab + (rr + 8 * i) * 64 + 16 * j + 4 * cc) = b;
+              }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::tma_store_2d(&tmC, slab, (int)colbase, (int)slab_y);
+              ptx::bulk_commit();
+            }
+            ++nout;
           }
-          emit(v0, v1, 1.0f, colbase + 64 * s, slab_y, split);
+        } else {
+#pragma unroll
+          for (int s = 0; s < kSlabs; ++s) {
+            float v0[32], v1[32];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              upk(acc[32 * s + j], v0[2 * j], v0[2 * j + 1]);
+              upk(acc[32 * s + 16 + j], v1[2 * j], v1[2 * j + 1]);
+            }
+            emit(v0, v1, 1.0f, colbase + 64 * s, slab_y, split);
+          }
         }
       }
     }
@@ -687,16 +767,18 @@ EncodeTiledFn encode_fn() {
 }
 
 // bf16 [rows, cols] row-major output, boxes of 32 rows x 64 columns (128 bytes),
-// 128-byte swizzle; out-of-range parts of a box are not written.
-bool make_out_map(CUtensorMap *m, void *base, int64_t rows, int64_t cols) {
+// 128-byte swizzle, or (narrow) 32 rows x 32 columns unswizzled; out-of-range
+// parts of a box are not written.
+bool make_out_map(CUtensorMap *m, void *base, int64_t rows, int64_t cols, bool narrow) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, 32};
+  cuuint32_t box[2] = {narrow ? 32u : 64u, 32};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            narrow ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -805,7 +887,7 @@ cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const C
   attr[0].val.clusterDim.x = kCl;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = st;
   cfg.attrs = attr;
@@ -883,7 +965,9 @@ cudaError_t launch_gemm(const uint8_t *A, int a_fmt, const float *a_sinv, const 
   if (!make_map(&ta, A, M, K, BM) || !make_map(&tb, B, N, K, p.pr ? p.bn / 2 : p.bn))
     return cudaErrorInvalidValue;
   if (p.splits == 1) {
-    if (!make_out_map(&tc, Cout, M, N)) return cudaErrorInvalidValue;
+    // the 1x128 x 1x128 kernel's epilogue warps own 32 columns each
+    if (!make_out_map(&tc, Cout, M, N, scaling == FP8_SCALING_1x128_1x128))
+      return cudaErrorInvalidValue;
   } else {
     tc = ta;  // unused by the split-K variant
   }

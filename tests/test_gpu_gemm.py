@@ -86,6 +86,14 @@ def test_gemm_tensor_ragged_tiles(fp, M, N, K):
     _run(fp, M, N, K, "tensor", "e5m2", "e4m3", seed=N + K)
 
 
+@pytest.mark.parametrize("M,N,K", [(4224, 304, 8192), (384, 256, 640), (2048, 512, 32768),
+                                   (1152, 1040, 2048)])
+def test_gemm_block_block_ragged(fp, M, N, K):
+    # 1x128 x 1x128 (wgrad scaling; 16 epilogue warps of 32 columns, 16x256b
+    # TMEM reads): an odd M tile count, ragged N and K tails, split-K (32768)
+    _run(fp, M, N, K, "1x128_1x128", "e5m2", "e4m3", seed=M + K)
+
+
 @pytest.mark.parametrize("afmt,bfmt", [("e4m3", "e4m3"), ("e5m2", "e4m3"), ("e4m3", "e5m2"),
                                        ("e5m2", "e5m2")])
 def test_gemm_formats(fp, afmt, bfmt):
