@@ -27,6 +27,8 @@
 //             4 transposed rows of 16 bytes (8 lanes = one 128-byte segment)
 // Ragged tails: the last tile may have fewer rows/columns (multiples of 16);
 // absent elements are zero-filled (zeros never raise an amax) and never stored.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -306,52 +308,55 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) xw[i] = *reinterpret_cast<const uint4 *>(&in[(rr + 16 * i) * 128 + 8 * cg]);
     // any inf or NaN among these 64 values selects the cast's NaN fix-up
-    const bool special = any_nonfinite64(xw);
+    // (1x128: found by the maxima pass)
+    bool special = MODE == Q_BLOCK1x128 ? false : any_nonfinite64(xw);
 
-    // ---- maxima: one pass over the tile with packed bf16 |max|
+    // ---- maxima: one pass over the tile
     float s_tile = ts;
-    uint32_t cm[4] = {0, 0, 0, 0};  // column maxima of this thread's 8 columns (pairs)
-    if (MODE != Q_TENSOR) {
-      uint32_t tm = 0;              // 128x128: running tile maximum (pair)
+    if (MODE == Q_BLOCK1x128) {
+      uint32_t cm[4];  // column maxima of this thread's 8 columns (bf16 pairs)
+      // rows rr+16i and rr+16(i+1): each row's maximum over this thread's 8
+      // columns, the two packed as one bf16 pair, reduced over the 16 lanes
+      // of the row group with 4 shuffles for both rows at once; then the two
+      // row groups of the warp combine their column maxima, stored per warp.
+      // EXACT: bf16 max that ignores NaN; otherwise unsigned 16-bit max of the
+      // magnitude bits (finite bf16 magnitudes order like unsigned integers).
+      auto maxima = [&](auto exact) {
+        constexpr bool kExact = decltype(exact)::value;
+        auto mx = [](uint32_t acc, uint32_t w) {
+          return kExact ? absmax2(acc, w) : __vmaxu2(acc, w & 0x7FFF7FFFu);
+        };
 #pragma unroll
-      for (int i = 0; i < 8; i += 2) {
-        if (MODE == Q_BLOCK1x128) {
-          // rows rr+16i and rr+16(i+1): each row's maximum over this thread's
-          // 8 columns, the two packed as one bf16 pair, reduced over the 16
-          // lanes of the row group with 4 shuffles for both rows at once
-          uint32_t m2[2];
+        for (int j = 0; j < 4; ++j) cm[j] = 0;
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+          uint32_t rm[2];  // per row: two partial maxima (the halves of the pair)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const uint4 w = xw[i + h];
-            cm[0] = absmax2(cm[0], w.x); cm[1] = absmax2(cm[1], w.y);
-            cm[2] = absmax2(cm[2], w.z); cm[3] = absmax2(cm[3], w.w);
-            const uint32_t rm = absmax2(absmax2(absmax2(absmax2(0u, w.x), w.y), w.z), w.w);
-            m2[h] = absmax2(rm, __byte_perm(rm, rm, 0x1032));  // both halves = row max
+            cm[0] = mx(cm[0], w.x); cm[1] = mx(cm[1], w.y);
+            cm[2] = mx(cm[2], w.z); cm[3] = mx(cm[3], w.w);
+            if (kExact)  // max with 0 drops NaN lanes
+              rm[h] = mx(mx(mx(mx(0u, w.x), w.y), w.z), w.w);
+            else
+              rm[h] = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
+                               __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
           }
-          uint32_t pr = __byte_perm(m2[0], m2[1], 0x7610);  // lo: row i, hi: row i+1
+          // lo: row i, hi: row i+1 (the max of each row's two halves)
+          uint32_t pr = mx(__byte_perm(rm[0], rm[1], 0x5410), __byte_perm(rm[0], rm[1], 0x7632));
 #pragma unroll
-          for (int o = 1; o < 16; o <<= 1) pr = absmax2(pr, __shfl_xor_sync(0xffffffffu, pr, o));
+          for (int o = 1; o < 16; o <<= 1) pr = mx(pr, __shfl_xor_sync(0xffffffffu, pr, o));
           if (cg == 0) {
             S.rowmx[rr + 16 * i] = __uint_as_float(pr << 16);
             S.rowmx[rr + 16 * (i + 1)] = __uint_as_float(pr & 0xFFFF0000u);
           }
-        } else {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint4 w = xw[i + h];
-            tm = absmax2(absmax2(absmax2(absmax2(tm, w.x), w.y), w.z), w.w);
-          }
         }
-      }
-      if (MODE == Q_BLOCK128) {
-        float a = bf16pair_max(tm);
+        // a magnitude >= 0x7F80 (inf or NaN) among this thread's 64 values
+        if (!kExact)
+          special = __vcmpgeu2(__vmaxu2(__vmaxu2(cm[0], cm[1]), __vmaxu2(cm[2], cm[3])),
+                               0x7F807F80u) != 0;
 #pragma unroll
-        for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-        if (lane == 0) S.red[warp] = a;
-      } else {
-        // combine the two row groups of the warp, then store per-warp column maxima
-#pragma unroll
-        for (int j = 0; j < 4; ++j) cm[j] = absmax2(cm[j], __shfl_xor_sync(0xffffffffu, cm[j], 16));
+        for (int j = 0; j < 4; ++j) cm[j] = mx(cm[j], __shfl_xor_sync(0xffffffffu, cm[j], 16));
         if (lane < 16 && want_col) {
           float4 *dst = reinterpret_cast<float4 *>(&S.colred[warp][8 * cg]);
           dst[0] = make_float4(__uint_as_float(cm[0] << 16), __uint_as_float(cm[0] & 0xFFFF0000u),
@@ -359,48 +364,64 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
           dst[1] = make_float4(__uint_as_float(cm[2] << 16), __uint_as_float(cm[2] & 0xFFFF0000u),
                                __uint_as_float(cm[3] << 16), __uint_as_float(cm[3] & 0xFFFF0000u));
         }
+      };
+      maxima(std::false_type{});
+      // NaN must not win a maximum: a tile holding inf or NaN anywhere redoes
+      // the maxima with the NaN-ignoring bf16 max (each thread rewrites the
+      // same shared entries it wrote above)
+      if (__syncthreads_or(special)) {
+        maxima(std::true_type{});
+        __syncthreads();
       }
-      __syncthreads();
-      if (MODE == Q_BLOCK128) {
+      // one division per thread: row scale of row t, column scale of column t
+      if (t < 128) {
+        float s, si;
+        scale_from_amax(S.rowmx[t], fmax, s, si);
+        S.rowsc[t] = s;
+        if (want_row && t < rows_here) {
+          p.row_scale[(r0 + t) * tiles_c + tc] = s;
+          p.row_scale_inv[(r0 + t) * tiles_c + tc] = si;
+        }
+      } else if (want_col) {
+        const int c = t - 128;
         float m = 0.0f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) m = fmaxf(m, S.red[w]);
-        float si;
-        scale_from_amax(m, fmax, s_tile, si);
-        if (t == 0) {
-          if (p.row_scale) {
-            p.row_scale[tr * tiles_c + tc] = s_tile;
-            p.row_scale_inv[tr * tiles_c + tc] = si;
-          }
-          if (p.col_scale) {
-            p.col_scale[tc * tiles_r + tr] = s_tile;
-            p.col_scale_inv[tc * tiles_r + tr] = si;
-          }
+        for (int w = 0; w < 8; ++w) m = fmaxf(m, S.colred[w][c]);
+        float s, si;
+        scale_from_amax(m, fmax, s, si);
+        S.colsc[c] = s;
+        if (c < cols_here) {
+          p.col_scale[(c0 + c) * tiles_r + tr] = s;
+          p.col_scale_inv[(c0 + c) * tiles_r + tr] = si;
         }
-      } else {
-        // one division per thread: row scale of row t, column scale of column t
-        if (t < 128) {
-          float s, si;
-          scale_from_amax(S.rowmx[t], fmax, s, si);
-          S.rowsc[t] = s;
-          if (want_row && t < rows_here) {
-            p.row_scale[(r0 + t) * tiles_c + tc] = s;
-            p.row_scale_inv[(r0 + t) * tiles_c + tc] = si;
-          }
-        } else if (want_col) {
-          const int c = t - 128;
-          float m = 0.0f;
+      }
+      __syncthreads();
+    } else if (MODE == Q_BLOCK128) {
+      uint32_t tm = 0;  // running tile maximum (bf16 pair)
 #pragma unroll
-          for (int w = 0; w < 8; ++w) m = fmaxf(m, S.colred[w][c]);
-          float s, si;
-          scale_from_amax(m, fmax, s, si);
-          S.colsc[c] = s;
-          if (c < cols_here) {
-            p.col_scale[(c0 + c) * tiles_r + tr] = s;
-            p.col_scale_inv[(c0 + c) * tiles_r + tr] = si;
-          }
+      for (int i = 0; i < 8; ++i) {
+        const uint4 w = xw[i];
+        tm = absmax2(absmax2(absmax2(absmax2(tm, w.x), w.y), w.z), w.w);
+      }
+      float a = bf16pair_max(tm);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+      if (lane == 0) S.red[warp] = a;
+      __syncthreads();
+      float m = 0.0f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) m = fmaxf(m, S.red[w]);
+      float si;
+      scale_from_amax(m, fmax, s_tile, si);
+      if (t == 0) {
+        if (p.row_scale) {
+          p.row_scale[tr * tiles_c + tc] = s_tile;
+          p.row_scale_inv[tr * tiles_c + tc] = si;
         }
-        __syncthreads();
+        if (p.col_scale) {
+          p.col_scale[tc * tiles_r + tr] = s_tile;
+          p.col_scale_inv[tc * tiles_r + tr] = si;
+        }
       }
     }
 
