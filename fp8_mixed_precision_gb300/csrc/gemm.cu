@@ -13,7 +13,8 @@
 //                             register accumulator (software promotion).
 //
 // Structure: persistent CTAs (one per SM), warp-specialised, tile BM x BN
-// (128 x 256 for tensor scaling when N allows, else 128 x 128).
+// (128 x 256 when N allows; 128 x 128 for narrow outputs and for
+// 1x128 x 1x128 scaling).
 //   warp 0      TMA producer: A (128 rows) and B (BN rows) tiles of 128 bytes
 //               along K, 128B swizzle, into a shared-memory ring guarded by
 //               full/empty mbarriers
@@ -22,7 +23,10 @@
 //   warps 2-9   epilogue: tcgen05.ld from TMEM, scale, round to bf16, stage
 //               32x64 slabs in 128B-swizzled shared memory, TMA bulk stores.
 //               Warp w reads TMEM lanes 32*(w%4)..+31 and column half (w-2)/4.
-//               (1x128 x 1x128: warps 2-17, column quarter (w-2)/4.)
+//   1x128 x 1x128: warps 2-17 are the epilogue, warp w taking column quarter
+//               (w-2)/4 of lanes 32*(w%4)..+31, read with the 16x256b shape
+//               (4 rows x 8 columns per thread) and staged as unswizzled
+//               32x32 slabs.
 // TMEM holds 512/BN accumulator buffers used round-robin, so the epilogue of
 // one tile (tensor scaling) or one K block (block scaling) overlaps the
 // following MMAs.  Deep-K tensor-scaled GEMMs use 256-row tiles (two M
@@ -253,11 +257,11 @@ __global__ void __launch_bounds__(Cfg<SCALING, SPLIT, BN, MH, PR>::kThreads, 1)
   constexpr int NB = C::kAccBufs;
   constexpr int kHalf = C::kCols;         // columns per epilogue warp
   constexpr int kSlabs = kHalf / 64;      // 64-column slabs per epilogue warp per tile
-  // block scaling: the partial is consumed in kCw-column TMEM loads (16 for
-  // 256-wide tiles, which keep 128 fp32 accumulators per thread in registers)
+  // 1x128 x 128x128 scaling: the partial is consumed in kCw-column TMEM
+  // loads (16 for 256-wide tiles, which keep 128 fp32 accumulators per
+  // thread in registers)
   constexpr int kCw = BN == 256 ? 16 : 32;
   constexpr int kChunks = kHalf / kCw;
-  constexpr int kBl = kHalf / 32;         // per-lane column scales (1x128 x 1x128)
   constexpr int kPre = BN == 256 ? 2 : 4; // K blocks of scales held ahead in registers
 
   extern __shared__ uint8_t smem_raw[];
@@ -592,20 +596,20 @@ __global__ void __launch_bounds__(Cfg<SCALING, SPLIT, BN, MH, PR>::kThreads, 1)
           }
           ptx::cp_async_wait_all();  // no scale copy in flight past the tile (abort path)
         } else {
-        float ra[kPre], rb[kPre][kBl];
-        auto load_scales = [&](int k, float &a, float (&b)[kBl]) {
+        float ra[kPre], rb[kPre];  // row scale, B tile scale
+        auto load_scales = [&](int k, float &a, float &b) {
           a = k < kb1 ? arow[k] : 0.0f;
-          b[0] = k < kb1 ? bt[k] : 0.0f;
+          b = k < kb1 ? bt[k] : 0.0f;
         };
 #pragma unroll
         for (int i = 0; i < kPre; ++i) load_scales(kb0 + i, ra[i], rb[i]);
         for (int kb = kb0; kb < kb1; ++kb) {
           const uint32_t ab = nacc % NB, aph = (nacc / NB) & 1;
-          const float sa_cur = ra[0], sbt_cur = rb[0][0];
+          const float sa_cur = ra[0], sbt_cur = rb[0];
 #pragma unroll
           for (int i = 0; i + 1 < kPre; ++i) {
             ra[i] = ra[i + 1];
-            rb[i][0] = rb[i + 1][0];
+            rb[i] = rb[i + 1];
           }
           load_scales(kb + kPre, ra[kPre - 1], rb[kPre - 1]);
           if (!wait_bar<PR>(&ctl->acc_full[ab], aph, abort)) { ok = false; break; }

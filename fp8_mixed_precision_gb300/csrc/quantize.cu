@@ -14,11 +14,14 @@
 // Thread t owns 8 consecutive columns (cg = t & 15) of 8 rows (rr = t >> 4,
 // rows rr + 16 i): 16 lanes cover one 256-byte row, so every shared read is
 // conflict-free and every rowwise store is a contiguous 128-byte segment.
-//   maxima    one pass with packed bf16 |max| (128x128: the tile maximum;
-//             1x128: row maxima over the 16 lanes of a row, column maxima
-//             over the CTA), then one IEEE division per thread forms the 128
-//             row scales and the 128 column scales (tensorwise: the scale
-//             comes from the first pass's partial maxima)
+//   maxima    one pass over the registers (128x128: the tile maximum with
+//             the NaN-ignoring packed bf16 max; 1x128: row maxima over the 16
+//             lanes of a row and column maxima over the CTA, as unsigned
+//             16-bit maxima of the magnitude bits, which also flag inf/NaN;
+//             a tile holding one redoes them with the bf16 max), then one
+//             IEEE division per thread forms the 128 row scales and the 128
+//             column scales (tensorwise: the scale comes from the first
+//             pass's partial maxima)
 //   cast      packed fp32 multiplies, saturating RNE conversion; the rowwise
 //             bytes are stored, the bytes of the transposed layout go to a
 //             swizzled 16 KB tile
