@@ -117,3 +117,46 @@ def test_host_pipeline_validation_without_gpu(L):
     assert L.fp8_host_pipeline_sync(None) == 1
     L.fp8_host_pipeline_destroy(None)
     assert L.fp8_launch_count() == n0
+
+
+def _gemm_splits(L, M, N, K, scaling):
+    import fp8_mixed_precision_gb300 as fp
+    ws = ctypes.c_size_t(0)
+    assert L.fp8_gemm_workspace_size(M, N, K, fp.SCALING[scaling], ctypes.byref(ws)) == 0
+    assert ws.value % (M * N * 4) == 0, (M, N, K, scaling, ws.value)
+    return ws.value // (M * N * 4)  # split-K partial sums are fp32 [splits, M, N]
+
+
+def test_gemm_plan_properties_without_gpu(L):
+    """The GEMM's kernel plan is host logic: its split count (read back
+    through the workspace size, fp32 [splits, M, N]) must give every split
+    at least one 4-block group of K (the block-scaled kernels load the scales
+    of 4 K blocks as one 16-byte vector from a split's first block), never
+    exceed 32, and depend on (M, N, K, scaling) alone."""
+    shapes = [(M, N, K) for M in (128, 512, 2048, 16384, 131072) for N in (128, 512, 2048, 14336)
+              for K in (128, 512, 4096, 16384, 131072) if M * N <= 131072 * 2048]
+    for scaling in ("tensor", "1x128_128x128", "1x128_1x128"):
+        for M, N, K in shapes:
+            s = _gemm_splits(L, M, N, K, scaling)
+            kbs = -(-K // 128)
+            assert s == 0 or 2 <= s <= 32, (M, N, K, scaling, s)
+            if s:
+                kbp = -(-kbs // s)
+                kbp = -(-kbp // 4) * 4  # splits start on 4-block groups
+                assert -(-kbs // kbp) == s and kbp % 4 == 0, (M, N, K, scaling, s)
+            assert _gemm_splits(L, M, N, K, scaling) == s  # same plan on every query
+
+
+def test_gemm_plan_of_the_benchmark_linears(L):
+    """The isolated-linear benchmark's GEMMs (N = 131072 tokens): the output-
+    bound fprop/dgrad GEMMs (K = 512 or 2048, 131072 rows) are not split;
+    the wgrads reduce over all 131072 tokens into few output tiles and are
+    split (the counts the step's launch list shows)."""
+    T = 131072
+    for K, O in ((512, 512), (512, 2048), (2048, 512), (512, 8192)):
+        assert _gemm_splits(L, T, O, K, "tensor") == 0   # fprop
+        assert _gemm_splits(L, T, K, O, "tensor") == 0   # dgrad
+    assert _gemm_splits(L, 512, 512, T, "tensor") == 16
+    assert _gemm_splits(L, 2048, 512, T, "tensor") == 9
+    assert _gemm_splits(L, 512, 2048, T, "tensor") == 9
+    assert _gemm_splits(L, 8192, 512, T, "tensor") == 2
