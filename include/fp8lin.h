@@ -34,6 +34,11 @@
  *     enqueues on its pipeline's own streams).  Arguments are validated before anything is
  *     launched: on a non-OK status nothing was enqueued.
  *   - Calls are not thread-safe with respect to one fp8_weight_cache object.
+ *     Other calls may come from several host threads: the per-device launch
+ *     settings the library fills in on first use (shared-memory opt-in,
+ *     resident CTA counts, SM count) are idempotent, so concurrent first
+ *     calls store the same values.  The kernel timing of fp8_profile_begin /
+ *     fp8_profile_end and the launch counter are process-wide.
  *
  * Recipes
  *   FP8_RECIPE_TENSORWISE: one current (just-in-time) amax per tensor.
