@@ -138,10 +138,12 @@ def test_stack_weight_cache_bitwise(fp, recipe):
         assert rel <= chain_tol(n), f"dW1[{l}] accumulated: relative Frobenius error {rel:.3g}"
 
 
-def test_large_block_linear_sampled_tiles(fp):
-    """fc1 of the large block-scaled MLP at full size (4096 -> 14336, 16384
-    tokens, 1% of X entries x100): GPU fwd + bwd, oracle on sampled tiles."""
-    N, K, O = 16384, 4096, 14336
+@pytest.mark.parametrize("K,O", [(4096, 14336), (14336, 4096)])
+def test_large_block_linear_sampled_tiles(fp, K, O):
+    """fc1 (4096 -> 14336) and fc2 (14336 -> 4096) of the large block-scaled
+    MLP at full size (16384 tokens, 1% of X entries x100): GPU fwd + bwd,
+    oracle on sampled tiles of Y, dX and dW."""
+    N = 16384
     x = syn.bf16_normal((N, K), 1.0, syn.SEED_X, device="cuda", outlier_frac=0.01)
     w = syn.bf16_normal((O, K), 0.02, syn.SEED_W, device="cuda")
     dy = syn.bf16_normal((N, O), 1e-3, syn.SEED_DY, device="cuda")
