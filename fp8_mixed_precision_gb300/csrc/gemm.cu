@@ -60,6 +60,9 @@ struct SmemCtl {
   uint64_t full[kMaxStages], empty[kMaxStages];
   uint64_t acc_full[4], acc_empty[4];
   uint64_t mma_done;
+  // 128 x 256 1x128 x 1x128 tiles: the scale ring's slots (filled by the
+  // producer warp's cp.async, drained by the epilogue warps)
+  uint64_t sfull[4], sempty[4];
   uint32_t tmem_base;
   int abort;
   // 1x128 x 1x128 only: per epilogue warp, the column and row scales of the
@@ -71,6 +74,15 @@ struct SmemCtl {
 constexpr int kCtlFull = (int)((sizeof(SmemCtl) + 127) / 128 * 128);
 // barriers and flags only (the column-scale area serves 1x128 x 1x128 alone)
 constexpr int kCtlSmall = (int)((offsetof(SmemCtl, bscale) + 127) / 128 * 128);
+
+// 1x128 x 1x128 scaling with 128 x 256 tiles ("wide"): the row and column
+// scales of a group of 4 K blocks sit in a CTA-wide ring of kScaleSlots
+// slots, each [4 K blocks][128 row scales + 256 column scales] fp32.
+constexpr int kScaleGroup = 4;
+constexpr int kScaleSlots = 3;
+constexpr int kScaleRowStride = BM + 256;  // floats per K block in a slot
+constexpr int kScaleSlotFloats = kScaleGroup * kScaleRowStride;
+constexpr int kScaleRingBytes = kScaleSlots * kScaleSlotFloats * 4;
 
 // Per-CTA configuration.
 //   MH  M halves per tile: MH = 2 gives 256 x BN tiles made of two M = 128
@@ -91,27 +103,45 @@ constexpr int kCtlSmall = (int)((offsetof(SmemCtl, bscale) + 127) / 128 * 128);
 // (64 bytes per row, unswizzled) for 32-column warps.
 template <int SCALING, bool SPLIT, int BN, int MH = 1, bool PR = false>
 struct Cfg {
+  // 1x128 x 1x128 with 256-wide tiles: scale ring, 64 columns per epilogue
+  // warp, bf16 results stored from registers once per tile
+  static constexpr bool kWide = SCALING == FP8_SCALING_1x128_1x128 && BN == 256;
   static constexpr int kEpi = SCALING == FP8_SCALING_1x128_1x128 ? 16 : 8;  // epilogue warps
-  static constexpr int kThreads = 64 + 32 * kEpi;
+  // Control warps before the epilogue: producer, MMA issuer and, for wide
+  // tiles, two idle warps completing warpgroup 0.  Wide tiles run as 5 whole
+  // warpgroups launched at kLaunchRegs registers per thread; warpgroup 0
+  // then gives registers back (setmaxnreg.dec to kCtlRegs) and the four
+  // epilogue warpgroups take them (setmaxnreg.inc to kEpiRegs), which holds
+  // their 64 fp32 accumulators, the partial and the scales without spills.
+  static constexpr int kCtlWarps = kWide ? 4 : 2;
+  static constexpr int kThreads = 32 * (kCtlWarps + kEpi);
+  static constexpr int kLaunchRegs = 96, kCtlRegs = 40, kEpiRegs = 104;
   static constexpr int kCols = BN * 4 / kEpi;  // tile columns per epilogue warp
   static constexpr int kStageA = MH * BM * BK;  // bytes
   static constexpr int kStageB = (PR ? BN / 2 : BN) * BK;  // a pair CTA holds half of B
   static constexpr int kStageBytes = kStageA + kStageB;
   static constexpr int kAccBufs = (int)kTmemCols / BN;
-  static constexpr int kCtlBytes = SCALING == FP8_SCALING_1x128_1x128 ? kCtlFull : kCtlSmall;
+  static constexpr int kCtlBytes =
+      SCALING == FP8_SCALING_1x128_1x128 && !kWide ? kCtlFull : kCtlSmall;
+  static constexpr int kScaleBytes = kWide ? kScaleRingBytes : 0;
   static constexpr int kOutSlabBytes = kCols == 32 ? 32 * 64 : 32 * 128;
-  static constexpr int kOutSlabs = SPLIT ? 0 : (MH == 2 || kCols == 32 ? 1 : 2);
+  static constexpr int kOutSlabs = SPLIT || kWide ? 0 : (MH == 2 || kCols == 32 ? 1 : 2);
   static constexpr int kOutBytes = kEpi * kOutSlabs * kOutSlabBytes;
-  static constexpr int kRing = kSmemBudget - 1024 - kOutBytes - kCtlBytes;
+  static constexpr int kRing = kSmemBudget - 1024 - kOutBytes - kCtlBytes - kScaleBytes;
   static constexpr int kStages = kRing / kStageBytes < kMaxStages ? kRing / kStageBytes : kMaxStages;
   static constexpr size_t kSmemBytes =
-      1024 + (size_t)kStages * kStageBytes + (size_t)kOutBytes + kCtlBytes;
+      1024 + (size_t)kStages * kStageBytes + (size_t)kOutBytes + kCtlBytes + kScaleBytes;
   static_assert(kStages >= 2, "shared memory too small for the operand ring");
   static_assert(MH == 1 || (MH == 2 && kAccBufs == 2), "two M halves fill TMEM exactly");
   static_assert(kCols == 32 || kCols % 64 == 0, "epilogue column split");
-  static_assert(SCALING != FP8_SCALING_1x128_1x128 || (kCols == 32 && kEpi * 256 <= 4096 &&
-                                                        kEpi * 64 <= 1024),
+  static_assert(SCALING != FP8_SCALING_1x128_1x128 || kWide ||
+                    (kCols == 32 && kEpi * 256 <= 4096 && kEpi * 64 <= 1024),
                 "scale staging areas");
+  static_assert(!kWide || (kCols == 64 && MH == 1 && !PR && kAccBufs == 2), "wide 1x128 tiles");
+  // the register split never asks for more than the launch provides
+  static_assert(!kWide || (kThreads == 640 && 128 * kCtlRegs + 32 * kEpi * kEpiRegs <=
+                                                  kThreads * kLaunchRegs),
+                "register split");
 };
 
 __device__ unsigned g_gemm_status;
@@ -126,6 +156,7 @@ struct GemmArgs {
   void *out;             // bf16 C [M, N], or fp32 partials [splits, M, N]
   uint32_t idesc;
   int vec4;              // scale rows are 16-byte aligned in groups of 4 K blocks
+  int group_m;           // > 0: units run in groups of group_m M tiles (N tiles within a group)
 };
 
 
@@ -164,13 +195,25 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
 // Unit u = (M tile, N tile, K split); for a CTA pair (PR) the M index is a
 // pair of 128-row tiles and CTA `rank` takes tile 2 * pair + rank (which may
 // lie past the last M tile).
+// Tiles run N-tile fastest, or (group_m > 0, single CTAs) in groups of
+// group_m M tiles, M tile fastest within a group: the CTAs running at one
+// time then share few A and B tiles, which L2 serves to all of them.
 template <bool PR>
 __device__ __forceinline__ void decode_unit(const GemmArgs &g, int64_t u, uint32_t rank, int &tm,
                                             int &tn, int &kb0, int &kb1) {
   const int split = (int)(u % g.splits);
   const int64_t t = u / g.splits;
-  tm = PR ? (int)(t / g.tiles_n) * 2 + (int)rank : (int)(t / g.tiles_n);
-  tn = (int)(t % g.tiles_n);
+  if (!PR && g.group_m > 0) {
+    const int64_t per_group = (int64_t)g.group_m * g.tiles_n;
+    const int64_t m0 = t / per_group * g.group_m;
+    const int64_t rem = t % per_group;
+    const int64_t gm = min((int64_t)g.group_m, (int64_t)g.tiles_m - m0);  // last group may be short
+    tm = (int)(m0 + rem % gm);
+    tn = (int)(rem / gm);
+  } else {
+    tm = PR ? (int)(t / g.tiles_n) * 2 + (int)rank : (int)(t / g.tiles_n);
+    tn = (int)(t % g.tiles_n);
+  }
   kb0 = split * g.kb_per_split;
   kb1 = min(g.kbs, kb0 + g.kb_per_split);
 }
@@ -270,6 +313,8 @@ __global__ void __launch_bounds__(Cfg<SCALING, SPLIT, BN, MH, PR>::kThreads, 1)
   uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t *out_stage = smem + (size_t)kStages * C::kStageBytes;
   SmemCtl *ctl = reinterpret_cast<SmemCtl *>(out_stage + C::kOutBytes);
+  // wide 1x128 x 1x128 tiles: ring of scale slots after the control block
+  float *scale_ring = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ctl) + C::kCtlBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -282,13 +327,18 @@ __global__ void __launch_bounds__(Cfg<SCALING, SPLIT, BN, MH, PR>::kThreads, 1)
       ptx::mbar_init(&ctl->acc_empty[b], PR ? 2 * C::kEpi : C::kEpi);
     }
     ptx::mbar_init(&ctl->mma_done, 1);
+    if (C::kWide)
+      for (int sl = 0; sl < kScaleSlots; ++sl) {
+        ptx::mbar_init(&ctl->sfull[sl], 32);  // one cp.async arrival per producer lane
+        ptx::mbar_init(&ctl->sempty[sl], C::kEpi);
+      }
     ctl->abort = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmB);
-    if (!SPLIT) ptx::tma_prefetch_desc(&tmC);
+    if (!SPLIT && !C::kWide) ptx::tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     if (PR) {
@@ -306,7 +356,69 @@ __global__ void __launch_bounds__(Cfg<SCALING, SPLIT, BN, MH, PR>::kThreads, 1)
   const uint32_t tmem = ctl->tmem_base;
   volatile int *abort = &ctl->abort;
 
-  if (warp == 0) {
+  if (warp < C::kCtlWarps) {
+  // wide tiles: registers move from the control warpgroup to the epilogue
+  if constexpr (C::kWide) ptx::setmaxnreg_dec<C::kCtlRegs>();
+  if (warp == 0 && C::kWide) {
+    // ------------------------------------------------------------ producer (wide 1x128 x 1x128)
+    // Lane 0 issues the operand TMA loads.  At the start of every group of 4
+    // K blocks of a unit, all 32 lanes copy the group's 128 row scales and
+    // 256 column scales (4 K blocks each, transposed to [K block][row or
+    // column]) into the next ring slot with cp.async; each lane arrives on the
+    // slot's full barrier once its copies have landed.  Scales of rows or
+    // columns past the tensor and of K blocks past the unit read as zeros.
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t ngrp = 0;
+    int last_phase[kStages];
+    for (int s = 0; s < kStages; ++s) last_phase[s] = -1;
+    bool ok = true;
+    for (int64_t u = u0; ok && u < g.units; u += ustep) {
+      int tm, tn, kb0, kb1;
+      decode_unit<PR>(g, u, rank, tm, tn, kb0, kb1);
+      const int64_t m0 = (int64_t)tm * BM, n0 = (int64_t)tn * BN;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (((kb - kb0) % kScaleGroup) == 0) {
+          const uint32_t slot = ngrp % kScaleSlots;
+          const bool w = wait_bar(&ctl->sempty[slot], ((ngrp / kScaleSlots) & 1) ^ 1, abort);
+          if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+          float *dst = scale_ring + slot * kScaleSlotFloats;
+          for (int idx = lane; idx < kScaleRowStride; idx += 32) {
+            const bool is_row = idx < BM;
+            const int64_t rix = is_row ? m0 + idx : n0 + (idx - BM);
+            const bool rok = rix < (is_row ? g.M : g.N);
+            const float *src = is_row ? g.a_sinv + (rok ? rix : 0) * g.lds_a
+                                      : g.b_sinv + (rok ? rix : 0) * g.lds_b;
+#pragma unroll
+            for (int kk = 0; kk < kScaleGroup; ++kk) {
+              const int k = kb + kk;
+              const bool v = rok && k < kb1;
+              ptx::cp_async4(dst + kk * kScaleRowStride + idx, src + (v ? k : 0), v ? 4u : 0u);
+            }
+          }
+          ptx::cp_async_mbar_arrive(&ctl->sfull[slot]);
+          ++ngrp;
+        }
+        bool w = true;
+        if (lane == 0) {
+          w = wait_bar(&ctl->empty[stage], phase ^ 1, abort);
+          if (w) {
+            uint8_t *sa = smem + (size_t)stage * C::kStageBytes;
+            ptx::mbar_arrive_expect_tx(&ctl->full[stage], (uint32_t)C::kStageBytes);
+            ptx::tma_load_2d(sa, &tmA, &ctl->full[stage], kb * BK, (int)m0);
+            ptx::tma_load_2d(sa + C::kStageA, &tmB, &ctl->full[stage], kb * BK, (int)n0);
+            last_phase[stage] = (int)phase;
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) { ok = false; break; }
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
+      }
+    }
+    ptx::cp_async_wait_all();  // no scale copy in flight at exit
+    if (!ok && lane == 0)      // let every issued operand copy land before the CTA can exit
+      for (int s = 0; s < kStages; ++s)
+        if (last_phase[s] >= 0) drain_wait(&ctl->full[s], (uint32_t)last_phase[s]);
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int stage = 0;
@@ -411,15 +523,19 @@ __global__ void __launch_bounds__(Cfg<SCALING, SPLIT, BN, MH, PR>::kThreads, 1)
         ptx::mma_commit(&ctl->mma_done);
       drain_wait(&ctl->mma_done, 0);
     }
+  }
   } else {
     // ------------------------------------------------------------ epilogue
+    if constexpr (C::kWide) ptx::setmaxnreg_inc<C::kEpiRegs>();
+    const int ew = warp - C::kCtlWarps;  // epilogue warp index
     const int q = warp & 3;          // TMEM lane quarter this warp may access
-    const int h = (warp - 2) >> 2;   // column group of the tile (kHalf columns)
+    const int h = ew >> 2;           // column group of the tile (kHalf columns)
     const int r = q * 32 + lane;     // tile row owned by this thread
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * kHalf);
     uint32_t nacc = 0;
+    uint32_t ngrp = 0;  // scale-ring slots consumed (wide 1x128 x 1x128 tiles)
     uint32_t nout = 0;  // bf16 slabs this warp has handed to TMA stores
-    uint8_t *slabs = out_stage + (size_t)(warp - 2) * C::kOutSlabs * C::kOutSlabBytes;
+    uint8_t *slabs = out_stage + (size_t)ew * C::kOutSlabs * C::kOutSlabBytes;
     float s_tensor = 0.0f;
     if (SCALING == FP8_SCALING_TENSOR) s_tensor = __fmul_rn(g.a_sinv[0], g.b_sinv[0]);
     // TMEM buffer ab drained by this warp: tell the MMA issuer (the leader's
@@ -438,7 +554,7 @@ __global__ void __launch_bounds__(Cfg<SCALING, SPLIT, BN, MH, PR>::kThreads, 1)
       if constexpr (SPLIT) {
         store32_f32(g, split, slab_y + lane, col0, v0, scale);
         store32_f32(g, split, slab_y + lane, col0 + 32, v1, scale);
-      } else {
+      } else if constexpr (C::kOutSlabs > 0) {
         if (slab_y >= g.M || col0 >= g.N) return;  // slab entirely outside C
         uint8_t *slab = slabs + (nout % C::kOutSlabs) * C::kOutSlabBytes;
         // the store kOutSlabs slabs ago has finished reading this buffer
@@ -492,6 +608,97 @@ __global__ void __launch_bounds__(Cfg<SCALING, SPLIT, BN, MH, PR>::kThreads, 1)
           ++nacc;
         }
         if (!ok) break;
+      } else if constexpr (C::kWide) {
+        // Every element's scale is (row scale) x (column scale) of its K
+        // block, both read from the scale ring.  The partial is read with the
+        // 16x256b TMEM shape: thread (rr, cc) = (lane / 4, lane % 4) holds
+        // rows rr + 8i (i = 0..3) of the warp's 32-row quarter and columns
+        // 32ch + 8j + 2cc, +1 (ch = 0..1, j = 0..3) of its 64 columns;
+        // acc[8i + 4ch + j] is that column pair of row i.
+        const int rr = lane >> 2, cc = lane & 3;
+        uint64_t acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = 0;
+        bool ok = true;
+        for (int g0 = kb0; ok && g0 < kb1; g0 += kScaleGroup) {
+          const uint32_t slot = ngrp % kScaleSlots;
+          if (!wait_bar(&ctl->sfull[slot], (ngrp / kScaleSlots) & 1, abort)) { ok = false; break; }
+          const float *srow = scale_ring + slot * kScaleSlotFloats + q * 32 + rr;
+          const float *scol = scale_ring + slot * kScaleSlotFloats + BM + h * 64 + 2 * cc;
+#pragma unroll 1
+          for (int kk = 0; kk < kScaleGroup; ++kk) {
+            if (g0 + kk >= kb1) break;
+            const uint32_t ab = nacc % NB, aph = (nacc / NB) & 1;
+            if (!wait_bar(&ctl->acc_full[ab], aph, abort)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const float *sak = srow + kk * kScaleRowStride;  // row scales of this K block
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+              uint64_t sb[4];  // column-scale pairs of this thread's 4 column pairs in half ch
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float2 b2 =
+                    *reinterpret_cast<const float2 *>(scol + kk * kScaleRowStride + 32 * ch + 8 * j);
+                sb[j] = pk(b2.x, b2.y);
+              }
+#pragma unroll
+              for (int hb = 0; hb < 2; ++hb) {  // TMEM lanes q*32 + 16 hb .. +15
+                uint32_t raw[16];
+                ptx::tmem_ld16x256b_x4(tl + ((uint32_t)(16 * hb) << 16) + ab * BN + 32 * ch, raw);
+                ptx::tmem_ld_wait();
+                if (ch == 1 && hb == 1) {  // the partial is in registers: free the TMEM buffer
+                  ptx::tc_fence_before();
+                  __syncwarp();
+                  if (lane == 0) release_acc(ab);
+                }
+#pragma unroll
+                for (int ii = 0; ii < 2; ++ii) {
+                  const int i = 2 * hb + ii;  // row rr + 8i
+                  const float sa = sak[8 * i];
+                  const uint64_t sa2 = pk(sa, sa);
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    const uint64_t sc = mul2(sa2, sb[j]);
+                    acc[8 * i + 4 * ch + j] =
+                        fma2(pk(__uint_as_float(raw[4 * j + 2 * ii]),
+                                __uint_as_float(raw[4 * j + 2 * ii + 1])),
+                             sc, acc[8 * i + 4 * ch + j]);
+                  }
+                }
+              }
+            }
+            ++nacc;
+          }
+          __syncwarp();  // every lane's reads of the slot are done
+          if (lane == 0) ptx::mbar_arrive(&ctl->sempty[slot]);
+          ++ngrp;
+        }
+        if (!ok) break;
+        // results straight from registers (once per tile): rows
+        // slab_y0 + rr + 8i, columns colbase + 32ch + 8j + 2cc and +1 (N is
+        // even, so n < N covers n + 1)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int64_t mm = slab_y0 + rr + 8 * i;
+          if (mm >= g.M) continue;
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int64_t n = colbase + 32 * ch + 8 * j + 2 * cc;
+              if (n >= g.N) continue;
+              float x, y;
+              upk(acc[8 * i + 4 * ch + j], x, y);
+              if constexpr (SPLIT) {
+                *reinterpret_cast<float2 *>(static_cast<float *>(g.out) +
+                                            ((int64_t)split * g.M + mm) * g.N + n) =
+                    make_float2(x, y);
+              } else {
+                *reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(g.out) +
+                                                    mm * g.N + n) = __floats2bfloat162_rn(x, y);
+              }
+            }
+        }
       } else {
         const int64_t slab_y = slab_y0;
         uint64_t acc[kHalf / 2];  // kHalf fp32 accumulators as packed pairs
@@ -518,10 +725,10 @@ __global__ void __launch_bounds__(Cfg<SCALING, SPLIT, BN, MH, PR>::kThreads, 1)
           const bool nok = n_st < g.N;
           const float *brow = g.b_sinv + (nok ? n_st : g.N - 1) * g.lds_b;
           // per warp: current group as [K block][32 columns] and [K block][32 rows]
-          float *bsw = ctl->bscale + (warp - 2) * 256;
+          float *bsw = ctl->bscale + ew * 256;
           float *asw = bsw + 128;
           // cp.async staging, one group ahead: [lane] column scales, then [lane] row scales
-          float4 *stg = ctl->sstage + (warp - 2) * 64;
+          float4 *stg = ctl->sstage + ew * 64;
           // Scales move in groups of 4 K blocks; each lane copies the 4 scales
           // of its staging column and of row q*32 + lane with cp.async
           // (nothing held in registers while in flight).
@@ -861,8 +1068,8 @@ Plan plan_for(int64_t M, int64_t N, int64_t K, int bn, int mh) {
 // Kernel configuration as a function of (M, N, K, scaling) only.
 Plan make_plan(int64_t M, int64_t N, int64_t K, int scaling) {
   // 256-wide tiles halve the A re-reads and the per-SM operand traffic per
-  // flop; the 1x128 x 1x128 promotion needs per-column scales and stays 128-wide
-  const int bn = (N >= 256 && scaling != FP8_SCALING_1x128_1x128) ? 256 : 128;
+  // flop (the 1x128 x 1x128 kernel of that width takes its scales from a ring)
+  const int bn = N >= 256 ? 256 : 128;
   Plan p = plan_for(M, N, K, bn, 1);
   if (scaling == FP8_SCALING_TENSOR && bn == 256 && M > BM) {
     const Plan p2 = plan_for(M, N, K, bn, 2);
@@ -906,6 +1113,12 @@ cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const C
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
+    if (C::kWide) {  // the setmaxnreg split needs the launch allocation it was sized for
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, kernel);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs < C::kLaunchRegs) return cudaErrorInvalidConfiguration;
+    }
     int n = num_sms();
     if (PR) {
       int clusters = 0;
@@ -941,11 +1154,9 @@ cudaError_t launch_scaling(const CUtensorMap &ta, const CUtensorMap &tb, const C
       return split ? launch_variant<SCALING, true, 256, 2>(ta, tb, tc, g, st)
                    : launch_variant<SCALING, false, 256, 2>(ta, tb, tc, g, st);
   }
-  if constexpr (SCALING != FP8_SCALING_1x128_1x128) {
-    if (bn == 256)
-      return split ? launch_variant<SCALING, true, 256>(ta, tb, tc, g, st)
-                   : launch_variant<SCALING, false, 256>(ta, tb, tc, g, st);
-  }
+  if (bn == 256)
+    return split ? launch_variant<SCALING, true, 256>(ta, tb, tc, g, st)
+                 : launch_variant<SCALING, false, 256>(ta, tb, tc, g, st);
   return split ? launch_variant<SCALING, true, 128>(ta, tb, tc, g, st)
                : launch_variant<SCALING, false, 128>(ta, tb, tc, g, st);
 }
@@ -968,12 +1179,12 @@ cudaError_t launch_gemm(const uint8_t *A, int a_fmt, const float *a_sinv, const 
   // a CTA pair loads the B tile as two halves of bn / 2 rows
   if (!make_map(&ta, A, M, K, BM) || !make_map(&tb, B, N, K, p.pr ? p.bn / 2 : p.bn))
     return cudaErrorInvalidValue;
-  if (p.splits == 1) {
-    // the 1x128 x 1x128 kernel's epilogue warps own 32 columns each
+  if (p.splits == 1 && !(scaling == FP8_SCALING_1x128_1x128 && p.bn == 256)) {
+    // the 128-wide 1x128 x 1x128 kernel's epilogue warps own 32 columns each
     if (!make_out_map(&tc, Cout, M, N, scaling == FP8_SCALING_1x128_1x128))
       return cudaErrorInvalidValue;
   } else {
-    tc = ta;  // unused by the split-K variant
+    tc = ta;  // unused: split-K partials and wide 1x128 x 1x128 results are stored from registers
   }
   GemmArgs g;
   g.M = M;
@@ -993,6 +1204,12 @@ cudaError_t launch_gemm(const uint8_t *A, int a_fmt, const float *a_sinv, const 
   g.idesc = ptx::idesc_f8f6f4((uint32_t)a_fmt, (uint32_t)b_fmt, p.pr ? 2 * BM : BM, (uint32_t)p.bn);
   g.vec4 = (p.kbs % 4 == 0) && (reinterpret_cast<uintptr_t>(a_sinv) % 16 == 0) &&
            (reinterpret_cast<uintptr_t>(b_sinv) % 16 == 0);
+  // Wide 1x128 x 1x128 tiles stream both operands per 128-deep K block for
+  // the whole K range: grouping 16 M tiles keeps the concurrently running
+  // tiles' A and B blocks shared through L2.  Other GEMMs keep the N-tile
+  // fastest order (measured faster for the K = 512 shapes, whose output
+  // rows are then written across all N tiles at once).
+  g.group_m = (scaling == FP8_SCALING_1x128_1x128 && p.bn == 256) ? std::min(16, p.tiles_m) : 0;
   const bool split = p.splits > 1;
   cudaError_t e;
   switch (scaling) {
