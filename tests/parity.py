@@ -1,5 +1,8 @@
 """Comparison helpers shared by the GPU parity tests (no FP8 arithmetic here:
 the expected values always come from the oracle)."""
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -65,4 +68,24 @@ def check_gemm(got: torch.Tensor, ref_f64: np.ndarray, abs_f64: np.ndarray, K: i
         assert not hard.any(), (f"{what}: {int(hard.sum())} elements beyond 2 ulp and the fp32 "
                                 f"summation bound, first at {tuple(np.argwhere(hard)[0])}")
         assert over.mean() < 1e-3, f"{what}: {int(over.sum())} elements beyond 2 ulp"
-    return dict(rel_frob=float(rel), over_2ulp=int(over.sum()))
+    nz = ulp > 0
+    max_ulp = float(np.max(err[nz] / ulp[nz])) if nz.any() else 0.0
+    return dict(rel_frob=float(rel), over_2ulp=int(over.sum()), max_ulp=max_ulp,
+                elements=int(g.size))
+
+
+def log_margin(what: str, K: int, results) -> dict:
+    """Aggregate check_gemm results of one GEMM (several tiles): worst
+    relative Frobenius error, total elements beyond 2 ulp, worst ulp error.
+    Appended as one JSON line to the file named by FP8_PARITY_LOG, if set."""
+    results = list(results)
+    agg = dict(gemm=what, K=int(K), tiles=len(results),
+               elements=sum(r["elements"] for r in results),
+               rel_frob_max=max(r["rel_frob"] for r in results),
+               over_2ulp=sum(r["over_2ulp"] for r in results),
+               max_ulp=max(r["max_ulp"] for r in results))
+    path = os.environ.get("FP8_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(agg) + "\n")
+    return agg

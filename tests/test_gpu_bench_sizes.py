@@ -3,14 +3,18 @@
 bench.py runs it (one shared workspace and context, fp8_linear_fwd then
 fp8_linear_bwd), so every GEMM goes through the tile shape, split count and
 CTA-pair configuration the benchmark times.  The oracle computes each
-tensor's global amax itself, quantizes only the rows and columns that
-sampled 128x128 output tiles of Y, dX and dW need, and checks those tiles."""
+tensor's global amax itself, quantizes only the rows and columns that the
+sampled 128x128 output tiles need, and checks for every GEMM the first and
+the last tile and 64 seeded random tiles (all tiles of a smaller grid).
+The wgrad's tiles, each a reduction over all 131072 tokens, come from a
+product set of random tile rows and columns holding at least 64 tiles."""
 import numpy as np
 import pytest
 import torch
 
 import oracle as o
-from parity import check_gemm
+import sampled
+from parity import check_gemm, log_margin
 from fp8_mixed_precision_gb300 import synthetic as syn
 
 pytestmark = pytest.mark.gpu
@@ -36,6 +40,10 @@ def _q(bits, s, si, fmt):
     return o.decode(o.cast(o.bf16_to_f32(np.ascontiguousarray(bits)), s, fmt), fmt) * np.float64(si)
 
 
+def _sl(t):
+    return slice(t * 128, (t + 1) * 128)
+
+
 @pytest.mark.parametrize("layer,K,O", [(i, k, o_) for i, (k, o_) in enumerate(SHAPES)])
 def test_bench_linear_sampled_tiles(fp, layer, K, O):
     dev = torch.device("cuda")
@@ -57,20 +65,37 @@ def test_bench_linear_sampled_tiles(fp, layer, K, O):
     sw, swi = _scale(wb, "e4m3")
     sg, sgi = _scale(dyb, "e5m2")
     rng = np.random.default_rng(layer)
-    sl = lambda t: slice(t * 128, (t + 1) * 128)
-    tm_last, tn_last, tk_last = N // 128 - 1, O // 128 - 1, K // 128 - 1
-    picks = [(0, 0, 0), (tm_last, tn_last, tk_last),
-             (int(rng.integers(N // 128)), int(rng.integers(O // 128)), int(rng.integers(K // 128)))]
-    for tm, tn, tk in picks:
-        # Y tile (tm, tn): X rows x W rows, reduced over K
-        A = _q(xb[sl(tm)], sx, sxi, "e4m3")
-        B = _q(wb[sl(tn)], sw, swi, "e4m3")
-        check_gemm(y[sl(tm), sl(tn)], A @ B.T, np.abs(A) @ np.abs(B).T, K, f"Y tile {tm},{tn}")
-        # dX tile (tm, tk): dY rows x W columns, reduced over O
-        A = _q(dyb[sl(tm)], sg, sgi, "e5m2")
-        B = _q(wb[:, sl(tk)].T, sw, swi, "e4m3")
-        check_gemm(dx[sl(tm), sl(tk)], A @ B.T, np.abs(A) @ np.abs(B).T, O, f"dX tile {tm},{tk}")
-        # dW tile (tn, tk): dY columns x X columns, reduced over all N tokens
-        A = _q(dyb[:, sl(tn)].T, sg, sgi, "e5m2")
-        B = _q(xb[:, sl(tk)].T, sx, sxi, "e4m3")
-        check_gemm(dw[sl(tn), sl(tk)], A @ B.T, np.abs(A) @ np.abs(B).T, N, f"dW tile {tn},{tk}")
+    Wd = _q(wb, sw, swi, "e4m3")                     # [O, K], small: whole
+    Wa = np.abs(Wd)
+
+    # Y tiles (tm, tn): X rows x W rows, reduced over K
+    yt = sampled.tiles(N // 128, O // 128, rng)
+    rows = sorted({tm for tm, _ in yt})
+    Xr = dict(zip(rows, sampled.pmap(lambda tm: _q(xb[_sl(tm)], sx, sxi, "e4m3"), rows)))
+    res = [check_gemm(y[_sl(tm), _sl(tn)], Xr[tm] @ Wd[_sl(tn)].T,
+                      np.abs(Xr[tm]) @ Wa[_sl(tn)].T, K, f"Y tile {tm},{tn}") for tm, tn in yt]
+    log_margin(f"fprop {N}x{O}x{K} tensorwise", K, res)
+    del Xr
+
+    # dX tiles (tm, tk): dY rows x W columns, reduced over O
+    dt = sampled.tiles(N // 128, K // 128, rng)
+    rows = sorted({tm for tm, _ in dt})
+    Gr = dict(zip(rows, sampled.pmap(lambda tm: _q(dyb[_sl(tm)], sg, sgi, "e5m2"), rows)))
+    res = [check_gemm(dx[_sl(tm), _sl(tk)], Gr[tm] @ Wd[:, _sl(tk)],
+                      np.abs(Gr[tm]) @ Wa[:, _sl(tk)], O, f"dX tile {tm},{tk}") for tm, tk in dt]
+    log_margin(f"dgrad {N}x{K}x{O} tensorwise", O, res)
+    del Gr
+
+    # dW tiles (tn, tk): dY columns x X columns, reduced over all N tokens
+    rn, ck = sampled.tile_grid(O // 128, K // 128, rng)
+    Gc = dict(zip(rn, sampled.pmap(lambda tn: _q(dyb[:, _sl(tn)].T, sg, sgi, "e5m2"), rn)))
+    Xc = dict(zip(ck, sampled.pmap(lambda tk: _q(xb[:, _sl(tk)].T, sx, sxi, "e4m3"), ck)))
+    Xa = {tk: np.abs(v) for tk, v in Xc.items()}
+    res = []
+    for tn in rn:
+        A = Gc.pop(tn)
+        Aa = np.abs(A)
+        for tk in ck:
+            res.append(check_gemm(dw[_sl(tn), _sl(tk)], A @ Xc[tk].T, Aa @ Xa[tk].T, N,
+                                  f"dW tile {tn},{tk}"))
+    log_margin(f"wgrad {O}x{K}x{N} tensorwise", N, res)

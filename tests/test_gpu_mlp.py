@@ -8,8 +8,9 @@ import pytest
 import torch
 
 import oracle as o
+import sampled
 from fp8_mixed_precision_gb300 import synthetic as syn
-from parity import assert_bytes_equal, assert_f32_equal, check_gemm, to_np
+from parity import assert_bytes_equal, assert_f32_equal, bf16_ulp, check_gemm, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -142,7 +143,8 @@ def test_stack_weight_cache_bitwise(fp, recipe):
 def test_large_block_linear_sampled_tiles(fp, K, O):
     """fc1 (4096 -> 14336) and fc2 (14336 -> 4096) of the large block-scaled
     MLP at full size (16384 tokens, 1% of X entries x100): GPU fwd + bwd,
-    oracle on sampled tiles of Y, dX and dW."""
+    oracle on the first, the last and 64 seeded random 128x128 tiles of Y, dX
+    and dW."""
     N = 16384
     x = syn.bf16_normal((N, K), 1.0, syn.SEED_X, device="cuda", outlier_frac=0.01)
     w = syn.bf16_normal((O, K), 0.02, syn.SEED_W, device="cuda")
@@ -162,25 +164,14 @@ def test_large_block_linear_sampled_tiles(fp, K, O):
     assert_bytes_equal(e.col, wq["col"], "Wq col")
     assert_f32_equal(e.col_scale_inv, wq["col_scale_inv"], "Wq col scale_inv")
     rng = np.random.default_rng(3)
-    sl = lambda t: slice(t * 128, (t + 1) * 128)
-    for _ in range(3):
-        tm, tn, tk = int(rng.integers(N // 128)), int(rng.integers(O // 128)), int(rng.integers(K // 128))
-        # Y tile: X rows of tile tm (1x128 blocks along K), W rows of tile tn
-        xq = o.quantize_1x128(np.ascontiguousarray(xb[sl(tm)]), "e4m3")
-        A = o.dequantize(xq["row"], xq["row_scale_inv"], "e4m3")
-        B = o.dequantize(wq["row"][sl(tn)], wq["row_scale_inv"][tn:tn + 1], "e4m3")
-        check_gemm(y[sl(tm), sl(tn)], A @ B.T, np.abs(A) @ np.abs(B).T, K, f"Y tile {tm},{tn}")
-        # dX tile: dY rows of tile tm (1x128 blocks along O), W^T rows of tile tk
-        gq = o.quantize_1x128(np.ascontiguousarray(dyb[sl(tm)]), "e5m2")
-        A = o.dequantize(gq["row"], gq["row_scale_inv"], "e5m2")
-        B = o.dequantize(wq["col"][sl(tk)], wq["col_scale_inv"][tk:tk + 1], "e4m3")
-        check_gemm(dx[sl(tm), sl(tk)], A @ B.T, np.abs(A) @ np.abs(B).T, O, f"dX tile {tm},{tk}")
-        # dW tile: dY columns of tile tn and X columns of tile tk, 1x128 blocks along tokens
-        gc = o.quantize_1x128(np.ascontiguousarray(dyb[:, sl(tn)]), "e5m2")
-        xc = o.quantize_1x128(np.ascontiguousarray(xb[:, sl(tk)]), "e4m3")
-        A = o.dequantize(gc["col"], gc["col_scale_inv"], "e5m2")
-        B = o.dequantize(xc["col"], xc["col_scale_inv"], "e4m3")
-        check_gemm(dw[sl(tn), sl(tk)], A @ B.T, np.abs(A) @ np.abs(B).T, N, f"dW tile {tn},{tk}")
+    Wr = o.dequantize(wq["row"], wq["row_scale_inv"], "e4m3")    # fprop B [O, K]
+    Wc = o.dequantize(wq["col"], wq["col_scale_inv"], "e4m3")    # dgrad B [K, O]
+    # first, last and 64 random output tiles of each GEMM (X rows and dY rows
+    # in 1x128 blocks along the reduction; the wgrad's operands are the
+    # transposed layouts, 1x128 blocks along the 16384 tokens)
+    sampled.check_fwd_like(y, xb, "e4m3", Wr, K, f"fprop {N}x{O}x{K} block 1x128x128x128", rng)
+    sampled.check_fwd_like(dx, dyb, "e5m2", Wc, O, f"dgrad {N}x{K}x{O} block 1x128x128x128", rng)
+    sampled.check_wgrad(dw, dyb, "e5m2", xb, "e4m3", f"wgrad {O}x{K}x{N} block 1x128x1x128", rng)
 
 
 @pytest.mark.parametrize("N", [1024, 400])
@@ -199,6 +190,35 @@ def test_fused_gelu_quantize_equals_unfused(fp, N):
         assert torch.equal(got.row, exp["row"]) and torch.equal(got.col, exp["col"])
         for k in ("row_scale", "row_scale_inv", "col_scale", "col_scale_inv"):
             assert torch.equal(getattr(got, k).view(torch.int32), exp[k].view(torch.int32)), k
+
+
+@pytest.mark.parametrize("N,F", [(1024, 384), (400, 400)])
+def test_fused_gelu_quantize_oracle(fp, N, F):
+    """Quantization fused into the GELU producers against the oracle,
+    stage-wise (GELU is held to 1 bf16 ulp of the fp64 oracle, not bitwise):
+    the oracle's 1x128 quantizer, fed the GPU's bf16 GELU output (forward)
+    or dA * GELU'(H) (backward), gives the fused kernel's row and transposed
+    bytes and all four scale arrays bit for bit.  1% of H entries are x100
+    outliers; (400, 400) has ragged 128-blocks in both dimensions."""
+    h = syn.bf16_normal((N, F), 2.0, 83, device="cuda", outlier_frac=0.01)
+    da = syn.bf16_normal((N, F), 1e-3, 84, device="cuda")
+    qf = fp.fp8_gelu_quantize(h, fp.QuantizedTensor(N, F, "act", "cuda"))
+    gf = fp.fp8_gelu_bwd_quantize(da, h, fp.QuantizedTensor(N, F, "grad", "cuda"))
+    a = fp.fp8_gelu_fwd(h)
+    dh = fp.fp8_gelu_bwd(da, h)
+    torch.cuda.synchronize()
+    hb, dab = syn.bits(h), syn.bits(da)
+    for got_bf16, exp_bits, nm in ((a, o.gelu_fwd(hb), "GELU"), (dh, o.gelu_bwd(dab, hb), "GELU'")):
+        g = o.bf16_to_f32(syn.bits(got_bf16)).astype(np.float64)
+        e = o.bf16_to_f32(exp_bits).astype(np.float64)
+        assert (np.abs(g - e) <= bf16_ulp(e)).all(), f"{nm} beyond 1 bf16 ulp"
+    for q, stage, fmt, nm in ((qf, a, "e4m3", "fused GELU + quantize"),
+                              (gf, dh, "e5m2", "fused GELU backward + quantize")):
+        r = o.quantize_1x128(syn.bits(stage), fmt)
+        assert_bytes_equal(q.row, r["row"], f"{nm}: row bytes")
+        assert_bytes_equal(q.col, r["col"], f"{nm}: transposed bytes")
+        for k in ("row_scale", "row_scale_inv", "col_scale", "col_scale_inv"):
+            assert_f32_equal(getattr(q, k), r[k], f"{nm}: {k}")
 
 
 def test_fused_mlp_stack_equals_unfused(fp):
