@@ -11,8 +11,6 @@
 // fp8_quantize_tensorwise_noalloc keeps the scratch in a fixed device array
 // that is part of this library: every GPU that loads the library holds it
 // (kNoAllocPartials floats, 4 KiB) until the process exits.
-#include <mutex>
-
 #include "common.cuh"
 #include "internal.h"
 
@@ -27,26 +25,18 @@ constexpr int kNoAllocPartials = kMaxPartials;  // 1024 fp32 partial maxima
 // (different streams without ordering) race on it.
 static __device__ __align__(256) float g_noalloc_partials[kNoAllocPartials];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-float *g_partials_ptr[kMaxDevices] = {nullptr};
-
-// Device address of the array on the current device.  Host code must not use
-// the symbol itself (that is a host-side stand-in); the address is looked up
-// once per device, with that device current, on the device's first call.
+// Device address of the array in the current device's context.  Host code
+// must not use the symbol itself (that is a host-side stand-in).  The address
+// is looked up on every call, with the caller's device current: a context
+// that was torn down and created again (cudaDeviceReset, a released primary
+// context) loads the module anew and may place the array elsewhere, so a
+// remembered address could be stale.  The first call on a device also loads
+// the module there.
 cudaError_t partials_for_current_device(float **out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void *p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_partials);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_partials_ptr[dev]) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_partials);
-    if (e != cudaSuccess) return e;
-    g_partials_ptr[dev] = static_cast<float *>(p);
-  }
-  *out = g_partials_ptr[dev];
+  *out = static_cast<float *>(p);
   return cudaSuccess;
 }
 

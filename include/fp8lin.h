@@ -387,16 +387,18 @@ fp8_status fp8_host_pipeline_sync(fp8_host_pipeline *p);
  * Per-kernel timing for roofline reports.  Between fp8_profile_begin and
  * fp8_profile_end every kernel this library launches is bracketed by two
  * CUDA events recorded on its own launch stream, and the launcher's
- * algorithmic byte and flop counts for that launch are recorded with it.
- * fp8_profile_end synchronises those events and returns one record per
- * kernel name (at most `cap`; *n receives the number of distinct names).
- * Not thread-safe; host-side bookkeeping only. */
+ * algorithmic byte and flop counts and the problem shape of that launch are
+ * recorded with it.  fp8_profile_end synchronises those events and returns
+ * one record per kernel name and shape (at most `cap`; *n receives the
+ * number of distinct records).  Not thread-safe; host-side bookkeeping only. */
 typedef struct {
   char name[64];
   uint64_t launches;
   double total_ms;   /* sum of event-measured durations */
   double bytes;      /* sum of algorithmic HBM bytes (reads + writes) */
   double flops;      /* sum of algorithmic floating-point operations */
+  int64_t m, n, k;   /* shape: GEMM M, N, K (split-K reduce: M, N, splits);
+                        quantizers rows, cols, 0; elementwise kernels n, 0, 0 */
 } fp8_kernel_stat;
 
 fp8_status fp8_profile_begin(void);
@@ -416,9 +418,11 @@ fp8_status fp8_profile_end(fp8_kernel_stat *out, int cap, int *n);
  *   needs no workspace and makes no allocation; a launch that would need more
  *   than 1024 slots returns FP8_ERR_WORKSPACE (the first pass uses at most
  *   min(2 x SM count, 1024), so no supported size does).
- *   The first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   Every call looks up the array's device address (cudaGetSymbolAddress)
+ *   in the current device's context, so a context that was reset and
+ *   created again is handled; the first call on a device also loads the
+ *   library's device code there, so make that first call before any stream
+ *   capture.
  *   All calls on a device share the array and it keeps the last call's
  *   contents; each call overwrites every slot it reads, so nothing needs
  *   clearing.  Calls whose work can overlap on the GPU (unordered streams)
