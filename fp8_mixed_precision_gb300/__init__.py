@@ -114,7 +114,8 @@ _SIGS.update({
 class _KernelStat(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 64), ("launches", ctypes.c_uint64),
                 ("total_ms", ctypes.c_double), ("bytes", ctypes.c_double),
-                ("flops", ctypes.c_double)]
+                ("flops", ctypes.c_double), ("m", ctypes.c_int64), ("n", ctypes.c_int64),
+                ("k", ctypes.c_int64)]
 
 _lib = None
 
@@ -433,15 +434,26 @@ def fp8_profile_begin():
     _check(lib().fp8_profile_begin(), "fp8_profile_begin")
 
 
-def fp8_profile_end() -> list:
-    """Stop timing; one dict per kernel name: launches, total_ms, bytes, flops."""
-    cap = 64
+def fp8_profile_end(by_shape: bool = False) -> list:
+    """Stop timing; one dict per kernel name (by_shape: per kernel name and
+    launch shape) with launches, total_ms, bytes, flops (and m, n, k)."""
+    cap = 512
     arr = (_KernelStat * cap)()
     n = _c_int()
     _check(lib().fp8_profile_end(arr, cap, ctypes.byref(n)), "fp8_profile_end")
-    return [dict(name=arr[i].name.decode(), launches=int(arr[i].launches),
+    recs = [dict(name=arr[i].name.decode(), launches=int(arr[i].launches),
                  total_ms=float(arr[i].total_ms), bytes=float(arr[i].bytes),
-                 flops=float(arr[i].flops)) for i in range(min(n.value, cap))]
+                 flops=float(arr[i].flops), m=int(arr[i].m), n=int(arr[i].n), k=int(arr[i].k))
+            for i in range(min(n.value, cap))]
+    if by_shape:
+        return recs
+    agg = {}
+    for r in recs:
+        a = agg.setdefault(r["name"], dict(name=r["name"], launches=0, total_ms=0.0, bytes=0.0,
+                                           flops=0.0))
+        for key in ("launches", "total_ms", "bytes", "flops"):
+            a[key] += r[key]
+    return list(agg.values())
 
 
 def fp8_debug_wait_timeout(limit_ns: int, stream=None):

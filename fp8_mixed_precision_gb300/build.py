@@ -44,12 +44,15 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def _run(cmd, verbose):
+def _run(cmd, verbose, log=None):
     if verbose:
         print(" ".join(cmd), flush=True)
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"build failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
+    if log:
+        with open(log, "w") as f:
+            f.write(r.stdout + r.stderr)
     if verbose and (r.stdout or r.stderr):
         print(r.stdout + r.stderr, flush=True)
     return r
@@ -63,15 +66,16 @@ def build(force: bool = False, verbose: bool = False, extra_nvcc=()) -> str:
     nvcc = os.path.join(cuda, "bin", "nvcc")
     os.makedirs(BUILD, exist_ok=True)
     jobs = []
-    for f in CU_SOURCES:
+    for f in CU_SOURCES:   # ptxas resource report (registers, spills) kept beside the object
         obj = os.path.join(BUILD, f + ".o")
-        jobs.append([nvcc, *NVCC_FLAGS, *extra_nvcc, "-c", os.path.join(CSRC, f), "-o", obj])
+        jobs.append(([nvcc, *NVCC_FLAGS, "-Xptxas", "-v", *extra_nvcc, "-c", os.path.join(CSRC, f),
+                      "-o", obj], os.path.join(BUILD, f + ".ptxas.txt")))
     for f in CXX_SOURCES:
         obj = os.path.join(BUILD, f + ".o")
-        jobs.append(["g++", *CXX_FLAGS, "-I" + os.path.join(cuda, "include"), "-c",
-                     os.path.join(CSRC, f), "-o", obj])
+        jobs.append((["g++", *CXX_FLAGS, "-I" + os.path.join(cuda, "include"), "-c",
+                      os.path.join(CSRC, f), "-o", obj], None))
     with ThreadPoolExecutor(max_workers=min(8, len(jobs))) as ex:
-        list(ex.map(lambda c: _run(c, verbose), jobs))
+        list(ex.map(lambda c: _run(c[0], verbose, c[1]), jobs))
     objs = [os.path.join(BUILD, f + ".o") for f in CU_SOURCES + CXX_SOURCES]
     tmp = LIB + ".tmp"
     _run([nvcc, "-shared", *ARCH, "-o", tmp, *objs], verbose)

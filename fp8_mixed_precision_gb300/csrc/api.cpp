@@ -7,6 +7,7 @@
 #include <atomic>
 #include <cstring>
 #include <map>
+#include <tuple>
 #include <mutex>
 #include <new>
 #include <string>
@@ -25,6 +26,7 @@ struct ProfRec {
   const char *name;
   cudaEvent_t start, stop;
   double bytes, flops;
+  int64_t m, n, k;
 };
 std::mutex g_prof_mu;
 bool g_prof_on = false;
@@ -43,12 +45,13 @@ cudaEvent_t take_event() {
 }
 }  // namespace
 
-LaunchScope::LaunchScope(const char *name, cudaStream_t st, double bytes, double flops)
+LaunchScope::LaunchScope(const char *name, cudaStream_t st, double bytes, double flops, int64_t m,
+                         int64_t n, int64_t k)
     : st_(st) {
   count_launch();
   std::lock_guard<std::mutex> lk(g_prof_mu);
   if (!g_prof_on) return;
-  ProfRec r{name, take_event(), take_event(), bytes, flops};
+  ProfRec r{name, take_event(), take_event(), bytes, flops, m, n, k};
   if (!r.start || !r.stop) return;
   cudaEventRecord(r.start, st);
   g_prof.push_back(r);
@@ -697,7 +700,7 @@ fp8_status fp8_profile_begin(void) {
 fp8_status fp8_profile_end(fp8_kernel_stat *out, int cap, int *n) {
   std::lock_guard<std::mutex> lk(g_prof_mu);
   g_prof_on = false;
-  std::map<std::string, fp8_kernel_stat> agg;
+  std::map<std::tuple<std::string, int64_t, int64_t, int64_t>, fp8_kernel_stat> agg;
   fp8_status st = FP8_OK;
   for (auto &r : g_prof) {
     float ms = 0.0f;
@@ -706,10 +709,13 @@ fp8_status fp8_profile_end(fp8_kernel_stat *out, int cap, int *n) {
       st = FP8_ERR_CUDA;
       continue;
     }
-    fp8_kernel_stat &k = agg[r.name];
+    fp8_kernel_stat &k = agg[std::make_tuple(std::string(r.name), r.m, r.n, r.k)];
     if (k.launches == 0) {
       std::memset(&k, 0, sizeof(k));
       std::strncpy(k.name, r.name, sizeof(k.name) - 1);
+      k.m = r.m;
+      k.n = r.n;
+      k.k = r.k;
     }
     k.launches += 1;
     k.total_ms += ms;
@@ -869,9 +875,10 @@ fp8_status fp8_debug_wait_timeout(uint64_t limit_ns, fp8_stream_t stream) {
 }
 
 fp8_status fp8_get_device_status(fp8_stream_t stream) {
-  unsigned s = 0;
+  unsigned s = 0, q = 0;
   if (gemm_read_status(&s, cs(stream)) != cudaSuccess) return FP8_ERR_CUDA;
-  return (fp8_status)s;
+  if (quant_read_status(&q) != cudaSuccess) return FP8_ERR_CUDA;
+  return (fp8_status)(s ? s : q);
 }
 
 }  // extern "C"

@@ -75,14 +75,16 @@ constexpr int kCtlFull = (int)((sizeof(SmemCtl) + 127) / 128 * 128);
 // barriers and flags only (the column-scale area serves 1x128 x 1x128 alone)
 constexpr int kCtlSmall = (int)((offsetof(SmemCtl, bscale) + 127) / 128 * 128);
 
-// 1x128 x 1x128 scaling with 128 x 256 tiles ("wide"): the row and column
+// 1x128 x 1x128 scaling with 128 x 192 tiles ("wide"): the row and column
 // scales of a group of 4 K blocks sit in a CTA-wide ring of kScaleSlots
-// slots, each [4 K blocks][128 row scales + 256 column scales] fp32.
+// slots, each [4 K blocks][128 row scales + 192 column scales] fp32.
+constexpr int kWideBN = 192;
 constexpr int kScaleGroup = 4;
 constexpr int kScaleSlots = 3;
-constexpr int kScaleRowStride = BM + 256;  // floats per K block in a slot
+constexpr int kScaleRowStride = BM + kWideBN;  // floats per K block in a slot
 constexpr int kScaleSlotFloats = kScaleGroup * kScaleRowStride;
-constexpr int kScaleRingBytes = kScaleSlots * kScaleSlotFloats * 4;
+// ring slots, then the scale loaders' staging area (384 entries x 16 bytes)
+constexpr int kScaleRingBytes = kScaleSlots * kScaleSlotFloats * 4 + kScaleRowStride * 16;
 
 // Per-CTA configuration.
 //   MH  M halves per tile: MH = 2 gives 256 x BN tiles made of two M = 128
@@ -103,19 +105,20 @@ constexpr int kScaleRingBytes = kScaleSlots * kScaleSlotFloats * 4;
 // (64 bytes per row, unswizzled) for 32-column warps.
 template <int SCALING, bool SPLIT, int BN, int MH = 1, bool PR = false>
 struct Cfg {
-  // 1x128 x 1x128 with 256-wide tiles: scale ring, 64 columns per epilogue
-  // warp, bf16 results stored from registers once per tile
-  static constexpr bool kWide = SCALING == FP8_SCALING_1x128_1x128 && BN == 256;
-  static constexpr int kEpi = SCALING == FP8_SCALING_1x128_1x128 ? 16 : 8;  // epilogue warps
+  // 1x128 x 1x128 with 192-wide tiles: scale ring, 12 epilogue warps of 64
+  // columns, bf16 results stored from registers once per tile
+  static constexpr bool kWide = SCALING == FP8_SCALING_1x128_1x128 && BN == kWideBN;
+  static constexpr int kEpi =
+      kWide ? 12 : (SCALING == FP8_SCALING_1x128_1x128 ? 16 : 8);  // epilogue warps
   // Control warps before the epilogue: producer, MMA issuer and, for wide
-  // tiles, two idle warps completing warpgroup 0.  Wide tiles run as 5 whole
-  // warpgroups launched at kLaunchRegs registers per thread; warpgroup 0
-  // then gives registers back (setmaxnreg.dec to kCtlRegs) and the four
-  // epilogue warpgroups take them (setmaxnreg.inc to kEpiRegs), which holds
-  // their 64 fp32 accumulators, the partial and the scales without spills.
+  // tiles, the two scale-loader warps completing warpgroup 0.  Wide tiles run
+  // as 4 whole warpgroups launched at kLaunchRegs registers per thread;
+  // warpgroup 0 then gives registers back (setmaxnreg.dec to kCtlRegs) and
+  // the three epilogue warpgroups take them (setmaxnreg.inc to kEpiRegs),
+  // which holds their 64 fp32 accumulators, half a partial and its scales.
   static constexpr int kCtlWarps = kWide ? 4 : 2;
   static constexpr int kThreads = 32 * (kCtlWarps + kEpi);
-  static constexpr int kLaunchRegs = 96, kCtlRegs = 40, kEpiRegs = 104;
+  static constexpr int kLaunchRegs = 128, kCtlRegs = 32, kEpiRegs = 152;
   static constexpr int kCols = BN * 4 / kEpi;  // tile columns per epilogue warp
   static constexpr int kStageA = MH * BM * BK;  // bytes
   static constexpr int kStageB = (PR ? BN / 2 : BN) * BK;  // a pair CTA holds half of B
@@ -139,7 +142,7 @@ struct Cfg {
                 "scale staging areas");
   static_assert(!kWide || (kCols == 64 && MH == 1 && !PR && kAccBufs == 2), "wide 1x128 tiles");
   // the register split never asks for more than the launch provides
-  static_assert(!kWide || (kThreads == 640 && 128 * kCtlRegs + 32 * kEpi * kEpiRegs <=
+  static_assert(!kWide || (kThreads == 512 && 128 * kCtlRegs + 32 * kEpi * kEpiRegs <=
                                                   kThreads * kLaunchRegs),
                 "register split");
 };
@@ -199,22 +202,27 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
 // group_m M tiles, M tile fastest within a group: the CTAs running at one
 // time then share few A and B tiles, which L2 serves to all of them.
 template <bool PR>
-__device__ __forceinline__ void decode_unit(const GemmArgs &g, int64_t u, uint32_t rank, int &tm,
+__device__ __forceinline__ void decode_unit(const GemmArgs &g, int64_t u64, uint32_t rank, int &tm,
                                             int &tn, int &kb0, int &kb1) {
-  const int split = (int)(u % g.splits);
-  const int64_t t = u / g.splits;
+  // 32-bit arithmetic: the host refuses launches of 2^31 units or more (an
+  // output of over 2^45 elements), so every quotient here fits
+  const uint32_t u = (uint32_t)u64, splits = (uint32_t)g.splits;
+  const uint32_t split = u % splits;
+  const uint32_t t = u / splits;
+  const uint32_t tiles_n = (uint32_t)g.tiles_n;
   if (!PR && g.group_m > 0) {
-    const int64_t per_group = (int64_t)g.group_m * g.tiles_n;
-    const int64_t m0 = t / per_group * g.group_m;
-    const int64_t rem = t % per_group;
-    const int64_t gm = min((int64_t)g.group_m, (int64_t)g.tiles_m - m0);  // last group may be short
+    const uint32_t gmax = (uint32_t)g.group_m;
+    const uint32_t per_group = gmax * tiles_n;
+    const uint32_t m0 = t / per_group * gmax;
+    const uint32_t rem = t - (m0 / gmax) * per_group;
+    const uint32_t gm = min(gmax, (uint32_t)g.tiles_m - m0);  // last group may be short
     tm = (int)(m0 + rem % gm);
     tn = (int)(rem / gm);
   } else {
-    tm = PR ? (int)(t / g.tiles_n) * 2 + (int)rank : (int)(t / g.tiles_n);
-    tn = (int)(t % g.tiles_n);
+    tm = PR ? (int)(t / tiles_n) * 2 + (int)rank : (int)(t / tiles_n);
+    tn = (int)(t % tiles_n);
   }
-  kb0 = split * g.kb_per_split;
+  kb0 = (int)split * g.kb_per_split;
   kb1 = min(g.kbs, kb0 + g.kb_per_split);
 }
 
@@ -329,7 +337,7 @@ __global__ void __launch_bounds__(Cfg<SCALING, SPLIT, BN, MH, PR>::kThreads, 1)
     ptx::mbar_init(&ctl->mma_done, 1);
     if (C::kWide)
       for (int sl = 0; sl < kScaleSlots; ++sl) {
-        ptx::mbar_init(&ctl->sfull[sl], 32);  // one cp.async arrival per producer lane
+        ptx::mbar_init(&ctl->sfull[sl], 64);  // every lane of the two scale-loader warps
         ptx::mbar_init(&ctl->sempty[sl], C::kEpi);
       }
     ctl->abort = 0;
@@ -359,65 +367,65 @@ __global__ void __launch_bounds__(Cfg<SCALING, SPLIT, BN, MH, PR>::kThreads, 1)
   if (warp < C::kCtlWarps) {
   // wide tiles: registers move from the control warpgroup to the epilogue
   if constexpr (C::kWide) ptx::setmaxnreg_dec<C::kCtlRegs>();
-  if (warp == 0 && C::kWide) {
-    // ------------------------------------------------------------ producer (wide 1x128 x 1x128)
-    // Lane 0 issues the operand TMA loads.  At the start of every group of 4
-    // K blocks of a unit, all 32 lanes copy the group's 128 row scales and
-    // 256 column scales (4 K blocks each, transposed to [K block][row or
-    // column]) into the next ring slot with cp.async; each lane arrives on the
-    // slot's full barrier once its copies have landed.  Scales of rows or
-    // columns past the tensor and of K blocks past the unit read as zeros.
-    int stage = 0;
-    uint32_t phase = 0;
+  if (C::kWide && (warp == 2 || warp == 3)) {
+    // ------------------------------------------------------------ scale loaders (wide 1x128 x 1x128)
+    // For every group of 4 K blocks of a unit, the two warps copy the group's
+    // 128 row scales and 256 column scales (4 K blocks each: 16 bytes per row
+    // or column) into a staging area with cp.async (one 16-byte copy per row
+    // when the scale rows allow it), wait for their own copies, and store the
+    // values transposed, [K block][row or column], into the next ring slot;
+    // each lane then arrives on the slot's full barrier.  Rows or columns
+    // past the tensor and K blocks past the unit read as zeros.  A slot is
+    // reused once all epilogue warps released it.
+    const int part = warp - 2;                  // entries part*192 .. +191 of the 384
+    constexpr int kPer = kScaleRowStride / 2 / 32;
+    float4 *stg = reinterpret_cast<float4 *>(scale_ring + kScaleSlots * kScaleSlotFloats) +
+                  part * (kScaleRowStride / 2);
     uint32_t ngrp = 0;
-    int last_phase[kStages];
-    for (int s = 0; s < kStages; ++s) last_phase[s] = -1;
     bool ok = true;
     for (int64_t u = u0; ok && u < g.units; u += ustep) {
       int tm, tn, kb0, kb1;
       decode_unit<PR>(g, u, rank, tm, tn, kb0, kb1);
-      const int64_t m0 = (int64_t)tm * BM, n0 = (int64_t)tn * BN;
-      for (int kb = kb0; kb < kb1; ++kb) {
-        if (((kb - kb0) % kScaleGroup) == 0) {
-          const uint32_t slot = ngrp % kScaleSlots;
-          const bool w = wait_bar(&ctl->sempty[slot], ((ngrp / kScaleSlots) & 1) ^ 1, abort);
-          if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-          float *dst = scale_ring + slot * kScaleSlotFloats;
-          for (int idx = lane; idx < kScaleRowStride; idx += 32) {
-            const bool is_row = idx < BM;
-            const int64_t rix = is_row ? m0 + idx : n0 + (idx - BM);
-            const bool rok = rix < (is_row ? g.M : g.N);
-            const float *src = is_row ? g.a_sinv + (rok ? rix : 0) * g.lds_a
-                                      : g.b_sinv + (rok ? rix : 0) * g.lds_b;
+      const int m0 = tm * BM, n0 = tn * BN;
+      for (int g0 = kb0; g0 < kb1; g0 += kScaleGroup) {
+        const uint32_t slot = ngrp % kScaleSlots;
+        if (!wait_bar(&ctl->sempty[slot], ((ngrp / kScaleSlots) & 1) ^ 1, abort)) { ok = false; break; }
+        const bool whole = g.vec4 && g0 + kScaleGroup <= kb1;
+#pragma unroll 1
+        for (int e = 0; e < kPer; ++e) {
+          const int idx = part * (kScaleRowStride / 2) + e * 32 + lane;
+          const bool is_row = idx < BM;
+          const int rix = is_row ? m0 + idx : n0 + (idx - BM);
+          const bool rok = rix < (is_row ? g.M : g.N);
+          const float *src = (is_row ? g.a_sinv + (int64_t)(rok ? rix : 0) * g.lds_a
+                                     : g.b_sinv + (int64_t)(rok ? rix : 0) * g.lds_b) + g0;
+          if (whole) {
+            ptx::cp_async16_zfill(stg + e * 32 + lane, src, rok ? 16u : 0u);
+          } else {
+            float *d = reinterpret_cast<float *>(stg + e * 32 + lane);
 #pragma unroll
             for (int kk = 0; kk < kScaleGroup; ++kk) {
-              const int k = kb + kk;
-              const bool v = rok && k < kb1;
-              ptx::cp_async4(dst + kk * kScaleRowStride + idx, src + (v ? k : 0), v ? 4u : 0u);
+              const bool v = rok && g0 + kk < kb1;
+              ptx::cp_async4(d + kk, v ? src + kk : g.a_sinv, v ? 4u : 0u);
             }
           }
-          ptx::cp_async_mbar_arrive(&ctl->sfull[slot]);
-          ++ngrp;
         }
-        bool w = true;
-        if (lane == 0) {
-          w = wait_bar(&ctl->empty[stage], phase ^ 1, abort);
-          if (w) {
-            uint8_t *sa = smem + (size_t)stage * C::kStageBytes;
-            ptx::mbar_arrive_expect_tx(&ctl->full[stage], (uint32_t)C::kStageBytes);
-            ptx::tma_load_2d(sa, &tmA, &ctl->full[stage], kb * BK, (int)m0);
-            ptx::tma_load_2d(sa + C::kStageA, &tmB, &ctl->full[stage], kb * BK, (int)n0);
-            last_phase[stage] = (int)phase;
-          }
+        ptx::cp_async_commit();
+        ptx::cp_async_wait_all();  // this lane's copies have landed (it reads only its own)
+        float *dst = scale_ring + slot * kScaleSlotFloats;
+#pragma unroll 1
+        for (int e = 0; e < kPer; ++e) {
+          const int idx = part * (kScaleRowStride / 2) + e * 32 + lane;
+          const float4 v = stg[e * 32 + lane];
+          dst[0 * kScaleRowStride + idx] = v.x;
+          dst[1 * kScaleRowStride + idx] = v.y;
+          dst[2 * kScaleRowStride + idx] = v.z;
+          dst[3 * kScaleRowStride + idx] = v.w;
         }
-        if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) { ok = false; break; }
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        ptx::mbar_arrive(&ctl->sfull[slot]);
+        ++ngrp;
       }
     }
-    ptx::cp_async_wait_all();  // no scale copy in flight at exit
-    if (!ok && lane == 0)      // let every issued operand copy land before the CTA can exit
-      for (int s = 0; s < kStages; ++s)
-        if (last_phase[s] >= 0) drain_wait(&ctl->full[s], (uint32_t)last_phase[s]);
   } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -610,12 +618,11 @@ __global__ void __launch_bounds__(Cfg<SCALING, SPLIT, BN, MH, PR>::kThreads, 1)
         if (!ok) break;
       } else if constexpr (C::kWide) {
         // Every element's scale is (row scale) x (column scale) of its K
-        // block, both read from the scale ring.  The partial is read with the
-        // 16x256b TMEM shape: thread (rr, cc) = (lane / 4, lane % 4) holds
-        // rows rr + 8i (i = 0..3) of the warp's 32-row quarter and columns
-        // 32ch + 8j + 2cc, +1 (ch = 0..1, j = 0..3) of its 64 columns;
-        // acc[8i + 4ch + j] is that column pair of row i.
-        const int rr = lane >> 2, cc = lane & 3;
+        // block, both read from the scale ring.  Thread = row r of the tile
+        // (TMEM lane), 64 columns colbase .. +63; the partial is read with
+        // 32x32b loads of 8 columns, two in flight per wait, the column
+        // scales as broadcast 16-byte shared loads issued meanwhile, and
+        // acc[p] holds columns 2p, 2p + 1.
         uint64_t acc[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) acc[j] = 0;
@@ -623,49 +630,42 @@ __global__ void __launch_bounds__(Cfg<SCALING, SPLIT, BN, MH, PR>::kThreads, 1)
         for (int g0 = kb0; ok && g0 < kb1; g0 += kScaleGroup) {
           const uint32_t slot = ngrp % kScaleSlots;
           if (!wait_bar(&ctl->sfull[slot], (ngrp / kScaleSlots) & 1, abort)) { ok = false; break; }
-          const float *srow = scale_ring + slot * kScaleSlotFloats + q * 32 + rr;
-          const float *scol = scale_ring + slot * kScaleSlotFloats + BM + h * 64 + 2 * cc;
+          const float *ss = scale_ring + slot * kScaleSlotFloats;
 #pragma unroll 1
           for (int kk = 0; kk < kScaleGroup; ++kk) {
             if (g0 + kk >= kb1) break;
             const uint32_t ab = nacc % NB, aph = (nacc / NB) & 1;
             if (!wait_bar(&ctl->acc_full[ab], aph, abort)) { ok = false; break; }
             ptx::tc_fence_after();
-            const float *sak = srow + kk * kScaleRowStride;  // row scales of this K block
+            const float sa = ss[kk * kScaleRowStride + r];
+            const uint64_t sa2 = pk(sa, sa);
+            const float4 *sc4 =
+                reinterpret_cast<const float4 *>(ss + kk * kScaleRowStride + BM + h * 64);
+            // two halves of 32 columns: two 16-column TMEM loads in flight per
+            // wait, the halves' 32 column scales loaded from shared memory
+            // (broadcast 16-byte loads) and multiplied by the row scale meanwhile
 #pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-              uint64_t sb[4];  // column-scale pairs of this thread's 4 column pairs in half ch
+            for (int hf = 0; hf < 2; ++hf) {
+              uint32_t raw[32];
+              ptx::tmem_ld16(tl + ab * BN + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(raw));
+              ptx::tmem_ld16(tl + ab * BN + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(raw + 16));
+              uint64_t sc[16];  // row scale x column scale, column pairs 32 hf + 2 p, +1
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const float2 b2 =
-                    *reinterpret_cast<const float2 *>(scol + kk * kScaleRowStride + 32 * ch + 8 * j);
-                sb[j] = pk(b2.x, b2.y);
+              for (int v = 0; v < 8; ++v) {
+                const float4 b = sc4[8 * hf + v];
+                sc[2 * v] = mul2(sa2, pk(b.x, b.y));
+                sc[2 * v + 1] = mul2(sa2, pk(b.z, b.w));
+              }
+              ptx::tmem_ld_wait();
+              if (hf == 1) {  // the partial is in registers: free the TMEM buffer
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) release_acc(ab);
               }
 #pragma unroll
-              for (int hb = 0; hb < 2; ++hb) {  // TMEM lanes q*32 + 16 hb .. +15
-                uint32_t raw[16];
-                ptx::tmem_ld16x256b_x4(tl + ((uint32_t)(16 * hb) << 16) + ab * BN + 32 * ch, raw);
-                ptx::tmem_ld_wait();
-                if (ch == 1 && hb == 1) {  // the partial is in registers: free the TMEM buffer
-                  ptx::tc_fence_before();
-                  __syncwarp();
-                  if (lane == 0) release_acc(ab);
-                }
-#pragma unroll
-                for (int ii = 0; ii < 2; ++ii) {
-                  const int i = 2 * hb + ii;  // row rr + 8i
-                  const float sa = sak[8 * i];
-                  const uint64_t sa2 = pk(sa, sa);
-#pragma unroll
-                  for (int j = 0; j < 4; ++j) {
-                    const uint64_t sc = mul2(sa2, sb[j]);
-                    acc[8 * i + 4 * ch + j] =
-                        fma2(pk(__uint_as_float(raw[4 * j + 2 * ii]),
-                                __uint_as_float(raw[4 * j + 2 * ii + 1])),
-                             sc, acc[8 * i + 4 * ch + j]);
-                  }
-                }
-              }
+              for (int p = 0; p < 16; ++p)
+                acc[16 * hf + p] = fma2(pk(__uint_as_float(raw[2 * p]), __uint_as_float(raw[2 * p + 1])),
+                                        sc[p], acc[16 * hf + p]);
             }
             ++nacc;
           }
@@ -674,30 +674,37 @@ __global__ void __launch_bounds__(Cfg<SCALING, SPLIT, BN, MH, PR>::kThreads, 1)
           ++ngrp;
         }
         if (!ok) break;
-        // results straight from registers (once per tile): rows
-        // slab_y0 + rr + 8i, columns colbase + 32ch + 8j + 2cc and +1 (N is
-        // even, so n < N covers n + 1)
+        // results straight from registers (once per tile): row m, columns
+        // colbase .. +63 (N is a multiple of 16, so a 16-column group lies
+        // wholly inside or outside C)
+        if (m < g.M) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int64_t mm = slab_y0 + rr + 8 * i;
-          if (mm >= g.M) continue;
+          for (int c = 0; c < 4; ++c) {
+            const int64_t n = colbase + 16 * c;
+            if (n >= g.N) continue;
+            if constexpr (SPLIT) {
+              float *dst = static_cast<float *>(g.out) + ((int64_t)split * g.M + m) * g.N + n;
 #pragma unroll
-          for (int ch = 0; ch < 2; ++ch)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int64_t n = colbase + 32 * ch + 8 * j + 2 * cc;
-              if (n >= g.N) continue;
-              float x, y;
-              upk(acc[8 * i + 4 * ch + j], x, y);
-              if constexpr (SPLIT) {
-                *reinterpret_cast<float2 *>(static_cast<float *>(g.out) +
-                                            ((int64_t)split * g.M + mm) * g.N + n) =
-                    make_float2(x, y);
-              } else {
-                *reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(g.out) +
-                                                    mm * g.N + n) = __floats2bfloat162_rn(x, y);
+              for (int p = 0; p < 8; p += 2) {
+                float x0, y0, x1, y1;
+                upk(acc[8 * c + p], x0, y0);
+                upk(acc[8 * c + p + 1], x1, y1);
+                reinterpret_cast<float4 *>(dst)[p / 2] = make_float4(x0, y0, x1, y1);
               }
+            } else {
+              uint32_t w[8];
+#pragma unroll
+              for (int p = 0; p < 8; ++p) {
+                float x, y;
+                upk(acc[8 * c + p], x, y);
+                __nv_bfloat162 b = __floats2bfloat162_rn(x, y);
+                w[p] = *reinterpret_cast<uint32_t *>(&b);
+              }
+              uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(g.out) + m * g.N + n);
+              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
             }
+          }
         }
       } else {
         const int64_t slab_y = slab_y0;
@@ -1019,8 +1026,8 @@ struct Plan {
 struct TileRates {
   double sm, gpu;
 };
-constexpr TileRates kRatesBn128{14e12, 2.0e15}, kRatesBn256{20e12, 2.6e15},
-    kRatesBn256Mh2{23.5e12, 3.1e15};
+constexpr TileRates kRatesBn128{14e12, 2.0e15}, kRatesBn192{12e12, 1.9e15},
+    kRatesBn256{20e12, 2.6e15}, kRatesBn256Mh2{23.5e12, 3.1e15};
 constexpr double kPlanHbmBps = 6e12;   // fp32 split partials, written and read once
 constexpr double kPlanEpiBps = 60e9;   // per-SM epilogue drain rate (not overlapped, MH = 2)
 constexpr double kPlanReduceLaunchS = 4e-6;
@@ -1039,7 +1046,9 @@ Plan plan_for(int64_t M, int64_t N, int64_t K, int bn, int mh) {
   p.tiles_n = (int)((N + bn - 1) / bn);
   p.kbs = (int)((K + BK - 1) / BK);
   const int64_t tiles = (int64_t)p.tiles_m * p.tiles_n;
-  const TileRates r = bn == 128 ? kRatesBn128 : (mh == 2 ? kRatesBn256Mh2 : kRatesBn256);
+  const TileRates r = bn == 128 ? kRatesBn128
+                      : bn == kWideBN ? kRatesBn192
+                                      : (mh == 2 ? kRatesBn256Mh2 : kRatesBn256);
   const double kb_flops = 2.0 * BM * mh * bn * BK;
   const double all_s = (double)tiles * p.kbs * kb_flops / r.gpu;
   p.splits = 1;
@@ -1068,8 +1077,11 @@ Plan plan_for(int64_t M, int64_t N, int64_t K, int bn, int mh) {
 // Kernel configuration as a function of (M, N, K, scaling) only.
 Plan make_plan(int64_t M, int64_t N, int64_t K, int scaling) {
   // 256-wide tiles halve the A re-reads and the per-SM operand traffic per
-  // flop (the 1x128 x 1x128 kernel of that width takes its scales from a ring)
-  const int bn = N >= 256 ? 256 : 128;
+  // flop; under 1x128 x 1x128 scaling the tiles are 192 wide (the widest
+  // whose fp32 promotion fits the epilogue's registers), for outputs at least
+  // 320 wide (narrower ones would waste most of a second tile)
+  const int bn = scaling == FP8_SCALING_1x128_1x128 ? (N >= 320 ? kWideBN : 128)
+                                                    : (N >= 256 ? 256 : 128);
   Plan p = plan_for(M, N, K, bn, 1);
   if (scaling == FP8_SCALING_TENSOR && bn == 256 && M > BM) {
     const Plan p2 = plan_for(M, N, K, bn, 2);
@@ -1137,7 +1149,7 @@ cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const C
   double bytes = (double)g.M * g.K + (double)g.N * g.K + 2.0 * g.M * g.N;
   if (SCALING == FP8_SCALING_1x128_128x128) bytes += 4.0 * g.kbs * (g.M + (g.N + 127) / 128);
   if (SCALING == FP8_SCALING_1x128_1x128) bytes += 4.0 * g.kbs * (g.M + g.N);
-  LaunchScope ls(names[SCALING], st, bytes, 2.0 * g.M * g.N * g.K);
+  LaunchScope ls(names[SCALING], st, bytes, 2.0 * g.M * g.N * g.K, g.M, g.N, g.K);
   cfg.gridDim = dim3((unsigned)grid);
   return cudaLaunchKernelEx(&cfg, kernel, ta, tb, tc, g);
 }
@@ -1154,14 +1166,32 @@ cudaError_t launch_scaling(const CUtensorMap &ta, const CUtensorMap &tb, const C
       return split ? launch_variant<SCALING, true, 256, 2>(ta, tb, tc, g, st)
                    : launch_variant<SCALING, false, 256, 2>(ta, tb, tc, g, st);
   }
-  if (bn == 256)
+  if constexpr (SCALING == FP8_SCALING_1x128_1x128) {
+    if (bn == kWideBN)
+      return split ? launch_variant<SCALING, true, kWideBN>(ta, tb, tc, g, st)
+                   : launch_variant<SCALING, false, kWideBN>(ta, tb, tc, g, st);
+  } else if (bn == 256) {
     return split ? launch_variant<SCALING, true, 256>(ta, tb, tc, g, st)
                  : launch_variant<SCALING, false, 256>(ta, tb, tc, g, st);
+  }
   return split ? launch_variant<SCALING, true, 128>(ta, tb, tc, g, st)
                : launch_variant<SCALING, false, 128>(ta, tb, tc, g, st);
 }
 
 }  // namespace
+
+bool make_bf16_tile_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int box_rows,
+                        int box_cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int scaling) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
@@ -1179,7 +1209,7 @@ cudaError_t launch_gemm(const uint8_t *A, int a_fmt, const float *a_sinv, const 
   // a CTA pair loads the B tile as two halves of bn / 2 rows
   if (!make_map(&ta, A, M, K, BM) || !make_map(&tb, B, N, K, p.pr ? p.bn / 2 : p.bn))
     return cudaErrorInvalidValue;
-  if (p.splits == 1 && !(scaling == FP8_SCALING_1x128_1x128 && p.bn == 256)) {
+  if (p.splits == 1 && !(scaling == FP8_SCALING_1x128_1x128 && p.bn == kWideBN)) {
     // the 128-wide 1x128 x 1x128 kernel's epilogue warps own 32 columns each
     if (!make_out_map(&tc, Cout, M, N, scaling == FP8_SCALING_1x128_1x128))
       return cudaErrorInvalidValue;
@@ -1196,6 +1226,7 @@ cudaError_t launch_gemm(const uint8_t *A, int a_fmt, const float *a_sinv, const 
   g.splits = p.splits;
   g.kb_per_split = p.kb_per_split;
   g.units = (int64_t)(p.pr ? (p.tiles_m + 1) / 2 : p.tiles_m) * p.tiles_n * p.splits;
+  if (g.units >= (int64_t(1) << 31)) return cudaErrorInvalidValue;  // units are decoded in 32 bits
   g.a_sinv = a_sinv;
   g.b_sinv = b_sinv;
   g.lds_a = p.kbs;
@@ -1209,7 +1240,7 @@ cudaError_t launch_gemm(const uint8_t *A, int a_fmt, const float *a_sinv, const 
   // tiles' A and B blocks shared through L2.  Other GEMMs keep the N-tile
   // fastest order (measured faster for the K = 512 shapes, whose output
   // rows are then written across all N tiles at once).
-  g.group_m = (scaling == FP8_SCALING_1x128_1x128 && p.bn == 256) ? std::min(16, p.tiles_m) : 0;
+  g.group_m = (scaling == FP8_SCALING_1x128_1x128 && p.bn == kWideBN) ? std::min(16, p.tiles_m) : 0;
   const bool split = p.splits > 1;
   cudaError_t e;
   switch (scaling) {
@@ -1226,7 +1257,8 @@ cudaError_t launch_gemm(const uint8_t *A, int a_fmt, const float *a_sinv, const 
   if (e != cudaSuccess || !split) return e;
   const int64_t mn = M * N;
   const int64_t blocks = std::min<int64_t>((mn / 4 + 255) / 256, (int64_t)num_sms() * 8);
-  LaunchScope ls("gemm_splitk_reduce", st, 4.0 * p.splits * mn + 2.0 * mn, (double)p.splits * mn);
+  LaunchScope ls("gemm_splitk_reduce", st, 4.0 * p.splits * mn + 2.0 * mn, (double)p.splits * mn, M, N,
+                 p.splits);
   splitk_reduce_kernel<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, st>>>(
       static_cast<const float *>(ws), p.splits, mn, static_cast<__nv_bfloat16 *>(Cout));
   return cudaGetLastError();

@@ -64,7 +64,7 @@ unsigned grid_for(int64_t items) {
 
 cudaError_t launch_gelu_fwd(const void *H, void *A, int64_t n, cudaStream_t st) {
   const int64_t n8 = n / 8;
-  LaunchScope ls("gelu_fwd", st, 4.0 * n, 0.0);
+  LaunchScope ls("gelu_fwd", st, 4.0 * n, 0.0, n);
   gelu_fwd_kernel<<<grid_for(n8), kThreads, 0, st>>>(static_cast<const uint4 *>(H),
                                                       static_cast<uint4 *>(A), n8);
   return cudaGetLastError();
@@ -72,7 +72,7 @@ cudaError_t launch_gelu_fwd(const void *H, void *A, int64_t n, cudaStream_t st) 
 
 cudaError_t launch_gelu_bwd(const void *dA, const void *H, void *dH, int64_t n, cudaStream_t st) {
   const int64_t n8 = n / 8;
-  LaunchScope ls("gelu_bwd", st, 6.0 * n, 0.0);
+  LaunchScope ls("gelu_bwd", st, 6.0 * n, 0.0, n);
   gelu_bwd_kernel<<<grid_for(n8), kThreads, 0, st>>>(static_cast<const uint4 *>(dA),
                                                       static_cast<const uint4 *>(H),
                                                       static_cast<uint4 *>(dH), n8);
@@ -81,7 +81,7 @@ cudaError_t launch_gelu_bwd(const void *dA, const void *H, void *dH, int64_t n, 
 
 cudaError_t launch_grad_accumulate(float *acc, const void *dW, int64_t n, cudaStream_t st) {
   const int64_t n4 = n / 4;
-  LaunchScope ls("grad_accumulate", st, 10.0 * n, (double)n);
+  LaunchScope ls("grad_accumulate", st, 10.0 * n, (double)n, n);
   grad_accumulate_kernel<<<grid_for(n4), kThreads, 0, st>>>(
       reinterpret_cast<float4 *>(acc), static_cast<const uint2 *>(dW), n4);
   return cudaGetLastError();

@@ -2,6 +2,7 @@
 // kernel translation units.  Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (type only)
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stddef.h>
@@ -14,10 +15,14 @@ void count_launch();
 
 // Brackets one kernel launch with CUDA events on its stream while kernel
 // timing is enabled (fp8_profile_begin/end); also counts the launch.
-// bytes/flops: the launch's algorithmic HBM traffic and floating-point work.
+// bytes/flops: the launch's algorithmic HBM traffic and floating-point work;
+// m, n, k: its problem shape (GEMM M, N, K; quantizer rows, columns; glue
+// element count), which keeps launches of one kernel on different shapes
+// apart in the timing records.
 class LaunchScope {
  public:
-  LaunchScope(const char *name, cudaStream_t st, double bytes, double flops);
+  LaunchScope(const char *name, cudaStream_t st, double bytes, double flops, int64_t m = 0,
+              int64_t n = 0, int64_t k = 0);
   ~LaunchScope();
 
  private:
@@ -56,6 +61,14 @@ cudaError_t launch_gelu_quantize(const void *H, const void *H2, int64_t rows, in
                                  int bwd, uint8_t *out_row, uint8_t *out_col, float *row_scale,
                                  float *row_scale_inv, float *col_scale, float *col_scale_inv,
                                  cudaStream_t st);
+
+// TMA descriptor of a bf16 [rows, cols] row-major tensor (row stride cols,
+// 16-byte aligned base) for box_rows x box_cols boxes, no swizzle, zeros read
+// outside the tensor.
+bool make_bf16_tile_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int box_rows,
+                        int box_cols);
+// Reads and clears the quantizer kernels' device status word (0 = ok).
+cudaError_t quant_read_status(unsigned *status);
 
 // FP8 GEMM (tcgen05).  scaling: fp8_scaling.  ws may be null when
 // gemm_workspace_bytes() is 0.

@@ -9,8 +9,9 @@
 // gradients, 128x128 tiles for weights.
 //
 // Work decomposition (all modes): persistent CTAs of 256 threads, one 128x128
-// bf16 tile per loop iteration, staged in shared memory by cp.async into two
-// buffers so the next tile's load overlaps the current tile's work.
+// bf16 tile per loop iteration, staged in shared memory by one TMA tensor
+// load per tile into two buffers (completion on an mbarrier per buffer), so
+// the next tile's load overlaps the current tile's work.
 // Thread t owns 8 consecutive columns (cg = t & 15) of 8 rows (rr = t >> 4,
 // rows rr + 16 i): 16 lanes cover one 256-byte row, so every shared read is
 // conflict-free and every rowwise store is a contiguous 128-byte segment.
@@ -29,11 +30,14 @@
 //             32-bit shared loads), transposes it with byte permutes and writes
 //             4 transposed rows of 16 bytes (8 lanes = one 128-byte segment)
 // Ragged tails: the last tile may have fewer rows/columns (multiples of 16);
-// absent elements are zero-filled (zeros never raise an amax) and never stored.
+// absent elements are zero-filled by the TMA load (zeros never raise an amax)
+// and never stored.  Every wait on a tile is bounded: on expiry the kernel
+// records FP8_ERR_TIMEOUT in its status word and carries on (no trap).
 #include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace fp8lin {
 
@@ -108,8 +112,8 @@ struct QParams {
   float *cur_partials;    // delayed: per-CTA amax of this tensor, written by the cast pass
 };
 
-struct __align__(16) QSmem {
-  uint16_t in[2][128 * 128];  // bf16 tiles, 256 bytes per row
+struct __align__(128) QSmem {
+  uint16_t in[2][128 * 128];  // bf16 tiles, 256 bytes per row (TMA destinations)
   uint32_t tile[128 * 32];    // FP8 bytes for the transposed layout (swizzled words)
   float colred[8][128];       // 1x128: per-warp column maxima
   float colsc[128];           // 1x128: column scales
@@ -117,20 +121,26 @@ struct __align__(16) QSmem {
   float rowsc[128];           // 1x128: row scales
   float red[8];
   float tscale[2];
+  uint64_t full[2];           // TMA completion, one per tile buffer
 };
 constexpr size_t kQSmemBytes = sizeof(QSmem);
 
-__device__ __forceinline__ void cp_async16(void *dst, const void *src, bool valid) {
-  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src),
-               "r"(valid ? 16 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait1() {
-  asm volatile("cp.async.wait_group 1;" ::: "memory");
+__device__ unsigned g_quant_status;
+constexpr uint64_t kQWaitLimitNs = 2000000000ull;  // 2 s
+
+// Bounded wait for phase `parity` of a tile buffer's barrier.  On expiry the
+// status word records FP8_ERR_TIMEOUT and the caller proceeds (its results
+// are then invalid and the status reports it; nothing hangs or traps).
+__device__ __forceinline__ void wait_tile(uint64_t *bar, uint32_t parity) {
+  if (ptx::mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return;
+    if ((it & 63) == 0 && ptx::globaltimer() - t0 > kQWaitLimitNs) {
+      atomicCAS(&g_quant_status, 0u, (unsigned)FP8_ERR_TIMEOUT);
+      return;
+    }
+  }
 }
 
 // Eight fp32 values -> eight FP8 bytes (two little-endian words).  A product
@@ -191,16 +201,19 @@ __device__ __forceinline__ void unpack8(uint4 w, float (&v)[8]) {
   v[4] = bf16lo(w.z); v[5] = bf16hi(w.z); v[6] = bf16lo(w.w); v[7] = bf16hi(w.w);
 }
 
-// PRE selects a producer fused in front of the quantizer, applied to the
-// staged tile in shared memory and rounded to bf16 exactly as the standalone
-// kernels round (so fused and unfused results are bitwise equal):
+// PRE selects a producer fused in front of the quantizer, applied by each
+// thread to its own register tile of the staged input and rounded to bf16
+// exactly as the standalone kernels round (so fused and unfused results are
+// bitwise equal):
 //   0  none
 //   1  A = bf16(GELU(x))                 (activation of the next linear)
 //   2  dH = bf16(x * GELU'(x2)), x = dA  (gradient entering the linear below)
 template <int MODE, int FMT, int PRE = 0>
-__global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
+__global__ void __launch_bounds__(kQThreads, 2)
+    quant_tile_kernel(const __grid_constant__ CUtensorMap tmx,
+                      const __grid_constant__ CUtensorMap tmx2, QParams p) {
   static_assert(PRE == 0 || MODE == Q_BLOCK1x128, "fused producers use 1x128 blocks");
-  extern __shared__ uint8_t q_smem_raw[];
+  extern __shared__ __align__(1024) uint8_t q_smem_raw[];
   QSmem &S = *reinterpret_cast<QSmem *>(q_smem_raw);
 
   const float fmax = (FMT == FP8_FORMAT_E4M3) ? kE4M3Max : kE5M2Max;
@@ -209,24 +222,29 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
   const int64_t tiles_r = (p.R + 127) / 128, tiles_c = (p.C + 127) / 128;
   const int64_t ntiles = tiles_r * tiles_c;
 
-  // stage tile `id` of `src` into buffer b (zero fill outside the tensor)
-  auto stage = [&](const uint16_t *srcbase, int64_t id, int b) {
-    if (id < ntiles) {
-      const int64_t tr = (ntiles - 1 - id) / tiles_c, tc = (ntiles - 1 - id) % tiles_c;
-      const int64_t r0 = tr * 128, c0 = tc * 128;
-      const bool col_ok = c0 + 8 * cg < p.C;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = rr + 16 * i;
-        const bool ok = col_ok && r0 + r < p.R;
-        const uint16_t *src = ok ? srcbase + (r0 + r) * p.C + c0 + 8 * cg : srcbase;
-        cp_async16(&S.in[b][r * 128 + 8 * cg], src, ok);
-      }
-    }
-  };
+  if (t == 0) {
+    ptx::mbar_init(&S.full[0], 1);
+    ptx::mbar_init(&S.full[1], 1);
+    ptx::fence_mbar_init();
+    ptx::tma_prefetch_desc(&tmx);
+    if (PRE == 2) ptx::tma_prefetch_desc(&tmx2);
+  }
+  __syncthreads();
+  // Thread 0 loads tile `id` into buffer b with one TMA tensor load (two for
+  // the fused GELU backward: dA into buffer 0, H into buffer 1, both on
+  // barrier 0); parts of the box outside the tensor arrive as zeros.
   auto prefetch = [&](int64_t id, int b) {
-    if (PRE != 2) stage(p.x, id, b);
-    cp_async_commit();
+    if (t != 0 || id >= ntiles) return;
+    const int64_t tr = (ntiles - 1 - id) / tiles_c, tc = (ntiles - 1 - id) % tiles_c;
+    ptx::fence_proxy_async_smem();  // earlier generic writes to the buffer come first
+    if (PRE == 2) {
+      ptx::mbar_arrive_expect_tx(&S.full[0], 2u * 128 * 128 * 2);
+      ptx::tma_load_2d(S.in[0], &tmx, &S.full[0], (int)(tc * 128), (int)(tr * 128));
+      ptx::tma_load_2d(S.in[1], &tmx2, &S.full[0], (int)(tc * 128), (int)(tr * 128));
+    } else {
+      ptx::mbar_arrive_expect_tx(&S.full[b], 128u * 128 * 2);
+      ptx::tma_load_2d(S.in[b], &tmx, &S.full[b], (int)(tc * 128), (int)(tr * 128));
+    }
   };
 
   float ts = 1.0f, tsi = 1.0f;
@@ -264,7 +282,7 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
   uint32_t cur_max = 0;  // delayed: running |max| of this CTA's tiles (bf16 pair)
   int64_t id = blockIdx.x;
   prefetch(id, 0);
-  prefetch(id + gridDim.x, 1);
+  if (PRE != 2) prefetch(id + gridDim.x, 1);
   for (int k = 0; id < ntiles; ++k, id += gridDim.x) {
     const int b = PRE == 2 ? 0 : (k & 1);
     uint16_t *in = S.in[b];
@@ -273,21 +291,24 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
     const int rows_here = (int)(p.R - r0 < 128 ? p.R - r0 : 128);
     const int cols_here = (int)(p.C - c0 < 128 ? p.C - c0 : 128);
     const bool col_ok = 8 * cg < cols_here;
-    if (PRE == 2) {  // dA and H of this tile into the two buffers (no cross-tile overlap)
-      stage(p.x, id, 0);
-      stage(p.x2, id, 1);
-      cp_async_commit();
-      asm volatile("cp.async.wait_all;" ::: "memory");
-    } else {
-      cp_async_wait1();
-    }
-    __syncthreads();  // this tile is in shared memory for every thread
-    if (PRE != 0) {   // fused producer, in place, rounded to bf16
+    // this tile is in shared memory (fused GELU backward: dA and H, loaded
+    // after the previous tile finished, no cross-tile overlap)
+    if (PRE == 2)
+      wait_tile(&S.full[0], k & 1);
+    else
+      wait_tile(&S.full[b], (k >> 1) & 1);
+    // every thread has finished the previous tile's transpose reads of S.tile
+    // before this tile's cast writes it
+    __syncthreads();
+    // this thread's 8 rows x 8 columns of the tile, read from shared memory
+    // once and kept in registers for the maxima and the cast
+    uint4 xw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) xw[i] = *reinterpret_cast<const uint4 *>(&in[(rr + 16 * i) * 128 + 8 * cg]);
+    if (PRE != 0) {  // fused producer on the thread's own elements, rounded to bf16
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        uint4 *pw = reinterpret_cast<uint4 *>(&in[(rr + 16 * i) * 128 + 8 * cg]);
-        const uint4 w = *pw;
-        const uint32_t wi[4] = {w.x, w.y, w.z, w.w};
+        const uint32_t wi[4] = {xw[i].x, xw[i].y, xw[i].z, xw[i].w};
         uint32_t o4[4];
         if (PRE == 1) {
 #pragma unroll
@@ -300,16 +321,9 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
             o4[j] = pack_bf16x2(__fmul_rn(bf16lo(wi[j]), gelu_grad_f(bf16lo(hi4[j]))),
                                 __fmul_rn(bf16hi(wi[j]), gelu_grad_f(bf16hi(hi4[j]))));
         }
-        *pw = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+        xw[i] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
       }
-      __syncthreads();
     }
-
-    // this thread's 8 rows x 8 columns of the tile, read from shared memory
-    // once and kept in registers for the maxima and the cast
-    uint4 xw[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) xw[i] = *reinterpret_cast<const uint4 *>(&in[(rr + 16 * i) * 128 + 8 * cg]);
     // any inf or NaN among these 64 values selects the cast's NaN fix-up
     // (1x128: found by the maxima pass)
     bool special = MODE == Q_BLOCK1x128 ? false : any_nonfinite64(xw);
@@ -463,7 +477,10 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
       }
     }
     __syncthreads();  // tile complete; the bf16 buffer is free again
-    prefetch(id + 2 * (int64_t)gridDim.x, b);
+    if (PRE == 2)
+      prefetch(id + (int64_t)gridDim.x, 0);
+    else
+      prefetch(id + 2 * (int64_t)gridDim.x, b);
 
     // ---- transposed layout
     if (want_col) {
@@ -494,7 +511,6 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(QParams p) {
       }
     }
   }
-  asm volatile("cp.async.wait_all;" ::: "memory");  // no copy in flight at exit
   if (MODE == Q_TENSOR && p.cur_partials) {
     float a = bf16pair_max(cur_max);
 #pragma unroll
@@ -554,6 +570,13 @@ int tensorwise_partials_count(int64_t rows, int64_t cols) {
 
 template <int MODE, int FMT, int PRE = 0>
 static cudaError_t launch_tile(const QParams &p, cudaStream_t st) {
+  CUtensorMap tmx, tmx2;
+  if (!make_bf16_tile_map(&tmx, p.x, p.R, p.C, 128, 128)) return cudaErrorInvalidValue;
+  if (PRE == 2) {
+    if (!make_bf16_tile_map(&tmx2, p.x2, p.R, p.C, 128, 128)) return cudaErrorInvalidValue;
+  } else {
+    tmx2 = tmx;
+  }
   static const char *names[3] = {"quant_cast_tensorwise", "quant_block_1x128", "quant_block_128x128"};
   static const char *pre_names[3] = {"", "gelu_quant_block_1x128", "gelu_bwd_quant_block_1x128"};
   static bool attr_set[64] = {false};
@@ -579,15 +602,22 @@ static cudaError_t launch_tile(const QParams &p, cudaStream_t st) {
   else
     bytes += 16.0;
   if (PRE == 2) bytes += 2.0 * p.R * p.C;  // the second input (H)
-  LaunchScope ls(PRE ? pre_names[PRE] : names[MODE], st, bytes, 0.0);
-  quant_tile_kernel<MODE, FMT, PRE><<<(unsigned)grid, kQThreads, kQSmemBytes, st>>>(p);
+  LaunchScope ls(PRE ? pre_names[PRE] : names[MODE], st, bytes, 0.0, p.R, p.C);
+  quant_tile_kernel<MODE, FMT, PRE><<<(unsigned)grid, kQThreads, kQSmemBytes, st>>>(tmx, tmx2, p);
   return cudaGetLastError();
+}
+
+cudaError_t quant_read_status(unsigned *status) {
+  cudaError_t e = cudaMemcpyFromSymbol(status, g_quant_status, sizeof(unsigned));
+  if (e != cudaSuccess) return e;
+  const unsigned zero = 0;
+  return cudaMemcpyToSymbol(g_quant_status, &zero, sizeof(unsigned));
 }
 
 cudaError_t launch_amax_partials(const void *x, int64_t rows, int64_t cols, float *partials,
                                  cudaStream_t st) {
   const int g = tensorwise_partials_count(rows, cols);
-  LaunchScope ls("quant_amax_tensorwise", st, 2.0 * rows * cols, 0.0);
+  LaunchScope ls("quant_amax_tensorwise", st, 2.0 * rows * cols, 0.0, rows, cols);
   amax_partials_kernel<<<g, kAmaxThreads, 0, st>>>(static_cast<const uint4 *>(x), rows * cols / 8,
                                                    partials);
   return cudaGetLastError();

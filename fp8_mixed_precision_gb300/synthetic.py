@@ -2,13 +2,17 @@
 CPU oracle.  Holds no FP8 arithmetic: it only draws numbers.
 
 Recipe (the isolated-linear and MLP workloads): X ~ N(0, 1), W ~ N(0, 0.02),
-dY ~ N(0, 1e-3) (second parameter = standard deviation), drawn in float32 with
-torch's seeded generator, multiplied by the standard deviation in float32,
-then rounded once to bf16.  Outliers: a seeded permutation picks
-floor(frac * numel) distinct entries, which are multiplied by `factor` in
-float32 before the single bf16 rounding.
+dY ~ N(0, 1e-3) (second parameter = standard deviation), drawn in float32
+with torch's seeded CPU generator, multiplied by the standard deviation in
+float32, then rounded once to bf16.  Outliers: a seeded permutation (CPU
+generator) picks floor(frac * numel) distinct entries, which are multiplied
+by `factor` in float32 before the single bf16 rounding.  Every draw happens
+on the host and the bytes are then copied to the requested device, so the
+same seed gives the same tensor on any machine, with or without a GPU.
 """
 from __future__ import annotations
+
+import hashlib
 
 import numpy as np
 import torch
@@ -18,20 +22,31 @@ SEED_X, SEED_W, SEED_DY, SEED_OUTLIER = 42, 43, 44, 45
 
 def bf16_normal(shape, std: float, seed: int, device="cpu",
                 outlier_frac: float = 0.0, outlier_factor: float = 100.0) -> torch.Tensor:
-    """bf16 tensor of N(0, std) samples, reproducible from `seed`."""
-    g = torch.Generator(device=device)
+    """bf16 tensor of N(0, std) samples, reproducible from `seed` (drawn on
+    the host, then placed on `device`)."""
+    g = torch.Generator(device="cpu")
     g.manual_seed(int(seed))
-    x = torch.randn(tuple(shape), generator=g, dtype=torch.float32, device=device)
+    x = torch.randn(tuple(shape), generator=g, dtype=torch.float32)
     x.mul_(float(std))
     if outlier_frac > 0:
         n = x.numel()
         k = int(np.floor(outlier_frac * n))
-        g2 = torch.Generator(device=device)
+        g2 = torch.Generator(device="cpu")
         g2.manual_seed(SEED_OUTLIER)
-        idx = torch.randperm(n, generator=g2, device=device)[:k]
+        idx = torch.randperm(n, generator=g2)[:k]
         flat = x.view(-1)
         flat[idx] = flat[idx] * float(outlier_factor)
-    return x.to(torch.bfloat16)
+    x = x.to(torch.bfloat16)
+    return x if torch.device(device).type == "cpu" else x.to(device)
+
+
+def sha256(t: torch.Tensor) -> str:
+    """SHA-256 of a tensor's bytes (row-major, host copy), for recording
+    exactly which inputs a measurement used."""
+    a = t.detach().contiguous().cpu()
+    if a.dtype == torch.bfloat16:
+        a = a.view(torch.int16)
+    return hashlib.sha256(memoryview(a.numpy()).cast("B")).hexdigest()
 
 
 def bits(t: torch.Tensor) -> np.ndarray:

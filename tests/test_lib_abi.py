@@ -160,3 +160,28 @@ def test_gemm_plan_of_the_benchmark_linears(L):
     assert _gemm_splits(L, 2048, 512, T, "tensor") == 9
     assert _gemm_splits(L, 512, 2048, T, "tensor") == 9
     assert _gemm_splits(L, 8192, 512, T, "tensor") == 2
+
+
+def test_gemm_kernels_compile_without_spills(L):
+    """Register budget of the 1x128 x 1x128 GEMM kernels (the wgrad of the
+    block recipe): ptxas reports no spills for any of their instantiations
+    (the promotion epilogue holds its fp32 accumulators in registers, and its
+    register split between warpgroups is tight; a spill there costs a
+    local-memory round trip per K block).  Read from the resource report the
+    build keeps."""
+    log = os.path.join(ROOT, "fp8_mixed_precision_gb300", "_build", "gemm.cu.ptxas.txt")
+    if not os.path.exists(log):
+        from fp8_mixed_precision_gb300 import build
+        build.build(force=True)
+    txt = open(log).read()
+    blocks = re.split(r"Compiling entry function '", txt)[1:]
+    seen = 0
+    for b in blocks:
+        name = b.split("'", 1)[0]
+        if "fp8_gemm_kernelILi2E" not in name:   # scaling template argument 2 = 1x128 x 1x128
+            continue
+        seen += 1
+        m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", b)
+        assert m, name
+        assert m.group(1) == "0" and m.group(2) == "0", f"{name}: {m.group(0)}"
+    assert seen >= 4, seen
