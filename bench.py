@@ -40,14 +40,55 @@ FP8_OVER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate ratio (4.5 / 2.25 P
 
 
 def _peaks():
+    """HBM copy bandwidth and dense FP8 tensor peaks (burst: a kernel timed
+    alone at full clocks; sustained: a seconds-long loop under the power
+    cap), FP8 taken as the measured bf16 GEMM rate x the nominal FP8/BF16
+    ratio."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
-                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
-                    source="measured")
-    return dict(FALLBACK_PEAKS, source="fallback")
+        pk = dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                  bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                  source="measured")
+    else:
+        pk = dict(FALLBACK_PEAKS, source="fallback")
+    pk["fp8_tflops"] = pk["bf16_tflops"] * FP8_OVER_BF16
+    pk["fp8_tflops_sustained"] = pk["bf16_tflops_sustained"] * FP8_OVER_BF16
+    return pk
+
+
+def roofline_of(recs, steps: int, peaks: dict) -> dict:
+    """Per-instantiation rooflines from the library's per-launch event timing
+    (records per kernel name and launch shape).  Each launch is bounded by
+    max(flops / FP8 peak, bytes / HBM peak); its bound is the larger term.
+    Fractions are against the burst FP8 peak (this region is sub-second at
+    full clocks) and, beside it, the sustained one."""
+    fb, fs, hbm = peaks["fp8_tflops"], peaks["fp8_tflops_sustained"], peaks["hbm_gbs"]
+    tot = sum(r["total_ms"] for r in recs) or 1.0
+    inst, roof_ms = [], 0.0
+    for r in recs:
+        n = r["launches"]
+        t = r["total_ms"] / n / 1e3                       # seconds per launch
+        fl, by = r["flops"] / n, r["bytes"] / n
+        t_fl, t_by = fl / (fb * 1e12), by / (hbm * 1e9)
+        roof_ms += n * max(t_fl, t_by) * 1e3 / steps
+        if fl > 0 and t_fl >= t_by:
+            e = {"bound": "tensor", "achieved": fl / t / 1e12, "unit": "TFLOP/s",
+                 "peak_burst": fb, "peak_sustained": fs}
+        else:
+            e = {"bound": "hbm", "achieved": by / t / 1e9, "unit": "GB/s",
+                 "peak_burst": hbm, "peak_sustained": hbm}
+        e.update(kernel=r["name"], shape=[r["m"], r["n"], r["k"]],
+                 launches_per_step=n / steps, ms_per_launch=t * 1e3,
+                 share=r["total_ms"] / tot, frac_burst=e["achieved"] / e["peak_burst"],
+                 frac_sustained=e["achieved"] / e["peak_sustained"],
+                 roofline_ms_per_launch=max(t_fl, t_by) * 1e3,
+                 frac_of_roofline_time=max(t_fl, t_by) / t,
+                 traffic=_traffic_for(r["name"], (r["m"], r["n"], r["k"])))
+        inst.append(e)
+    inst.sort(key=lambda e: -e["share"])
+    return {"instances": inst, "roofline_ms_per_step": roof_ms}
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -130,44 +171,172 @@ def barrier(world: int):
 
 
 # ----------------------------------------------------------------------------- oracle timing
-def oracle_tokens_per_s(n_sample: int, repeats: int = 1) -> tuple[float, float]:
-    """Time the CPU oracle's linear fwd+bwd over the four shapes on n_sample
-    tokens each; returns (tokens/s, seconds)."""
+# The CPU oracle, as it stands, timed on the host cores.  Each measurement runs
+# in a fresh interpreter whose BLAS thread count is fixed before numpy loads,
+# so `cores` states the threads actually used: 1 (single thread) or every
+# host core (the oracle's numpy elementwise work - quantizers, encode - is
+# single-threaded by nature, so the all-core figures run independent samples
+# side by side on a thread pool, numpy releasing the interpreter lock, with
+# BLAS on all cores for the fp64 GEMMs).
+def _oracle_env(threads: int) -> dict:
+    env = dict(os.environ)
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(threads)
+    return env
+
+
+def run_oracle_timing(threads: int, spec: dict, timeout: float = 600.0) -> dict:
+    """Run oracle_timing_worker(spec) in a fresh interpreter with `threads`
+    BLAS threads; returns its JSON result."""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-timing",
+                        json.dumps(dict(spec, threads=threads))],
+                       env=_oracle_env(threads), capture_output=True, text=True, timeout=timeout)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle timing failed: {r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def oracle_timing_worker(spec: dict) -> dict:
+    """CPU oracle timings on bounded samples of each workload (called in the
+    subprocess).  Every figure names its sample; figures scaled from a
+    sample to the full workload say "extrapolated"."""
+    from concurrent.futures import ThreadPoolExecutor
+    import numpy as np
     import oracle as o
     from fp8_mixed_precision_gb300 import synthetic as syn
-    inputs = []
+    T = int(spec["threads"])
+    pool = ThreadPoolExecutor(max_workers=T)
+    bits = lambda t: syn.bits(t)
+    out = {"threads": T}
+
+    def par(fn, items):
+        return list(pool.map(fn, items)) if T > 1 else [fn(x) for x in items]
+
+    def clock(fn):
+        t0 = time.perf_counter()
+        r = fn()
+        return time.perf_counter() - t0, r
+
+    # -- isolated linears (headline workload): n tokens per linear, all four shapes;
+    # all-core: T independent samples of n tokens at once
+    n = int(spec.get("c1_tokens", 1024))
+    lin = []
     for i, (K, O) in enumerate(SHAPES):
-        x, w, dy = syn.linear_inputs(n_sample, K, O, layer=i)
-        inputs.append((syn.bits(x), syn.bits(w), syn.bits(dy)))
-    t0 = time.perf_counter()
-    for _ in range(repeats):
-        for x, w, dy in inputs:
-            o.linear_fwd_bwd(x, w, dy, RECIPE)
-    dt = time.perf_counter() - t0
-    return len(SHAPES) * n_sample * repeats / dt, dt
+        x, w, dy = syn.linear_inputs(n, K, O, layer=i)
+        lin.append((bits(x), bits(w), bits(dy)))
+    reps = max(1, T)
+    one_step = lambda: par(lambda _: [o.linear_fwd_bwd(x, w, dy, RECIPE) for x, w, dy in lin],
+                           range(reps))
+    for _ in range(int(spec.get("warmup", 0))):
+        one_step()
+    steps = max(1, int(spec.get("steps", 1)))
+    dt, _ = clock(lambda: [one_step() for _ in range(steps)])
+    out["c1"] = {"tokens_per_s": steps * reps * len(SHAPES) * n / dt, "seconds": dt,
+                 "steps": steps, "sample": f"{reps} x {n} tokens per linear, four shapes"}
+    if spec.get("c1_only"):
+        return out
+    # -- one 512->512 linear at N = 2048 (the whole workload), tensorwise
+    x, w, dy = syn.linear_inputs(2048, 512, 512)
+    xb, wb, dyb = bits(x), bits(w), bits(dy)
+    dt, _ = clock(lambda: o.linear_fwd_bwd(xb, wb, dyb, "tensorwise"))
+    out["c0"] = {"ms": 1e3 * dt, "tokens_per_s": 2048 / dt, "sample": "whole workload",
+                 "input_sha256": {"X": syn.sha256(x), "W": syn.sha256(w), "dY": syn.sha256(dy)}}
+    # -- block MLP d=512/ffn=2048 (fc1, GELU, fc2; fwd + bwd) on a token sample
+    nb = int(spec.get("mlp_tokens", 512))
+    d, ffn = 512, 2048
+    xs = [bits(syn.bf16_normal((nb, d), 1.0, syn.SEED_X + i)) for i in range(reps)]
+    dys = [bits(syn.bf16_normal((nb, d), 1e-3, syn.SEED_DY + i)) for i in range(reps)]
+    w1 = bits(syn.bf16_normal((ffn, d), 0.02, 43))
+    w2 = bits(syn.bf16_normal((d, ffn), 0.02, 44))
+    dt, _ = clock(lambda: par(lambda i: o.mlp_fwd_bwd(xs[i], w1, w2, dys[i], "block"), range(reps)))
+    mlp_tps = reps * nb / dt
+    out["c2"] = {"tokens_per_s": mlp_tps, "ms_per_step_extrapolated": 1e3 * 131072 / mlp_tps,
+                 "sample": f"{reps} x {nb} tokens (linear in tokens: extrapolated to 131072)"}
+    # -- 8-layer stack, GA = 4: 32 block passes of 131072 tokens + 16 weight quantizations
+    dt_w, _ = clock(lambda: par(lambda w: o.quantize(w, "block", "weight"), [w1, w2] * 8))
+    step_s = 8 * 4 * 131072 / mlp_tps + dt_w
+    out["c3"] = {"ms_per_step_cached_extrapolated": 1e3 * step_s,
+                 "ms_per_step_uncached_extrapolated": 1e3 * (step_s + 3 * dt_w),
+                 "weight_quantize_ms_16": 1e3 * dt_w,
+                 "sample": "block-MLP rate above x 8 layers x 4 microbatches of 131072 tokens "
+                           "+ 16 weight quantizations (timed)"}
+    # -- large block MLP d=4096/ffn=14336, 16384 tokens: quantizers on row
+    # samples and GEMMs on whole 128x128 output tiles, scaled to the workload
+    N4, D4, F4 = 16384, 4096, 14336
+    rows = 128
+    xr = bits(syn.bf16_normal((rows, D4), 1.0, syn.SEED_X, outlier_frac=0.01))
+    fr = bits(syn.bf16_normal((rows, F4), 1e-3, syn.SEED_DY))
+    wr = bits(syn.bf16_normal((rows, D4), 0.02, syn.SEED_W))
+    tq = {}
+    tq["act_d"], _ = clock(lambda: o.quantize_1x128(xr, "e4m3"))
+    tq["act_f"], _ = clock(lambda: o.quantize_1x128(fr, "e4m3"))
+    tq["w"], _ = clock(lambda: o.quantize_128x128(wr, "e4m3"))
+    # activations and gradients: X, dY [N, d] and A, dH [N, ffn]; weights W1, W2 [ffn x d]
+    q_s = 2 * (N4 / rows) * tq["act_d"] + 2 * (N4 / rows) * tq["act_f"] + 2 * (F4 / rows) * tq["w"]
+    # one output tile per GEMM kind, timed on dequantized operands
+    def tile_time(kred):
+        a = np.random.default_rng(1).standard_normal((128, kred))
+        b = np.random.default_rng(2).standard_normal((128, kred))
+        t, _ = clock(lambda: a @ b.T)
+        return t
+    tiles = {"fprop1": (N4 // 128) * (F4 // 128), "fprop2": (N4 // 128) * (D4 // 128)}
+    g_s = 0.0
+    for kred, ntile in ((D4, tiles["fprop1"]), (F4, tiles["fprop2"]),     # fc1 / fc2 fprop
+                        (F4, tiles["fprop2"]), (D4, tiles["fprop1"]),     # fc2 / fc1 dgrad
+                        (N4, (F4 // 128) * (D4 // 128)), (N4, (D4 // 128) * (F4 // 128))):  # wgrads
+        g_s += ntile * tile_time(kred)
+    gelu_s, _ = clock(lambda: o.gelu_fwd(fr))
+    out["c4"] = {"ms_per_step_extrapolated": 1e3 * (q_s + g_s + 2 * (N4 / rows) * gelu_s),
+                 "quantize_ms_extrapolated": 1e3 * q_s, "gemm_ms_extrapolated": 1e3 * g_s,
+                 "tokens_per_s_extrapolated": N4 / (q_s + g_s + 2 * (N4 / rows) * gelu_s),
+                 "sample": "quantizers on 128-row samples, one whole 128x128 output tile per GEMM "
+                           "(fp64), GELU on a 128-row sample; scaled to the workload"}
+    # -- quantizer throughput at the workloads' shapes (algorithmic bytes: 6 B
+    # per element tensorwise, 4 B + scales per element for the block recipes)
+    qs = {}
+    for name, R, C, kind in (("tensorwise 131072x8192", 131072, 8192, "t"),
+                             ("1x128 131072x2048", 131072, 2048, "a"),
+                             ("1x128 16384x14336", 16384, 14336, "a"),
+                             ("128x128 14336x4096", 14336, 4096, "w")):
+        r = 256
+        xs_q = [bits(syn.bf16_normal((r, C), 1.0, 60 + i)) for i in range(reps)]
+        fn = {"t": lambda b: o.quantize_tensorwise(b, "e4m3"),
+              "a": lambda b: o.quantize_1x128(b, "e4m3"),
+              "w": lambda b: o.quantize_128x128(b, "e4m3")}[kind]
+        dt, _ = clock(lambda: par(fn, xs_q))
+        per_el = 6.0 if kind == "t" else 4.0 + (16.0 / 128 if kind == "a" else 0.0)
+        gbs = reps * r * C * per_el / dt / 1e9
+        qs[name] = {"GB/s": gbs, "ms_extrapolated": 1e3 * R * C * per_el / (gbs * 1e9),
+                    "sample": f"{reps} x {r} rows"}
+    out["quantizers"] = qs
+    return out
 
 
 def run_reference(args):
-    """--impl reference: the CPU oracle on bounded samples of the workload."""
+    """--impl reference: the CPU oracle on bounded samples of the workload,
+    every host core in use (independent samples on a thread pool, BLAS on
+    all cores), one step = one such sample."""
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    # bounded sample per step, so that warmup + steps stay within minutes
-    n_sample = 256
-    for _ in range(args.warmup):
-        oracle_tokens_per_s(n_sample)
-    tps, dt = oracle_tokens_per_s(n_sample, repeats=args.steps)
-    cores = os.cpu_count()
+    cores = os.cpu_count() or 1
+    # one worker process runs the warm-up and then the timed steps
+    r = run_oracle_timing(cores, {"c1_tokens": 256, "c1_only": True, "warmup": args.warmup,
+                                  "steps": args.steps})["c1"]
+    secs = r["seconds"]
+    tps = r["tokens_per_s"]
+    toks = tps * secs
     line = {
         "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": "isolated FP8 linear fwd+bwd, tensorwise, shapes "
                    "512->512/512->2048/2048->512/512->8192",
-                   "tokens_per_step": len(SHAPES) * n_sample, "recipe": RECIPE},
+                   "tokens_per_step": toks / args.steps, "recipe": RECIPE},
         "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{n_sample} tokens per linear per step (of {N_TOKENS})"},
+                         "sample": f"{cores} independent samples of 256 tokens per linear per "
+                                   f"step (of {N_TOKENS}), one per host thread"},
         "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -192,8 +361,10 @@ def run_ours(args):
     N = N_TOKENS
     cache = fp.WeightCache()
     layers = []
+    hashes = {}
     for i, (K, O) in enumerate(SHAPES):
         x, w, dy = syn.linear_inputs(N, K, O, device=dev, layer=i)
+        hashes[f"{K}->{O}"] = {"X": syn.sha256(x), "W": syn.sha256(w), "dY": syn.sha256(dy)}
         h = cache.register(w, RECIPE)
         layers.append(dict(K=K, O=O, x=x, w=w, dy=dy, h=h,
                            y=torch.empty((N, O), dtype=torch.bfloat16, device=dev),
@@ -325,7 +496,7 @@ def run_ours(args):
         eager_step()
     p1.record(stream)
     torch.cuda.synchronize()
-    kstats = fp.fp8_profile_end()
+    krecs = fp.fp8_profile_end(by_shape=True)
     profiled_ms_step = p0.elapsed_time(p1) / args.steps
     # the other schedule, for reference (same work, same results)
     other = step_serial if args.schedule == "overlap" else step_overlap
@@ -354,10 +525,17 @@ def run_ours(args):
     tokens_per_step = len(SHAPES) * N
     value = world * tokens_per_step / (ms_step / 1e3)
 
-    # ---- roofline of the dominant kernel
+    # ---- rooflines: every kernel instantiation (kernel x launch shape), the
+    # dominant one as the headline, and the whole step
     peaks = _peaks()
-    fp8_peak = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
-    kstats.sort(key=lambda k: -k["total_ms"])
+    rl = roofline_of(krecs, args.steps, peaks)
+    agg = {}
+    for r in krecs:
+        a = agg.setdefault(r["name"], dict(name=r["name"], launches=0, total_ms=0.0, bytes=0.0,
+                                           flops=0.0))
+        for key in ("launches", "total_ms", "bytes", "flops"):
+            a[key] += r[key]
+    kstats = sorted(agg.values(), key=lambda k: -k["total_ms"])
     tot_ms = sum(k["total_ms"] for k in kstats) or 1.0
     kernels = []
     for k in kstats:
@@ -367,45 +545,55 @@ def run_ours(args):
                         "ms_per_step": k["total_ms"] / args.steps,
                         "share": k["total_ms"] / tot_ms, "GB/s": gbs, "TFLOP/s": tfs,
                         "hbm_frac": gbs / peaks["hbm_gbs"]})
-    dom = kstats[0]
-    dom_t = dom["total_ms"] / dom["launches"] / 1e3
-    intensity = dom["flops"] / max(dom["bytes"], 1.0)
-    ridge = fp8_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if intensity > ridge:
-        achieved = dom["flops"] / dom["launches"] / dom_t / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s"}
-    else:
-        achieved = dom["bytes"] / dom["launches"] / dom_t / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["kernel"] = dom["name"]
-    roof["peak_source"] = peaks["source"] + (" sustained bf16 x 2" if roof["bound"] == "tensor"
-                                             else " copy bandwidth")
-    roof["traffic"] = _traffic_for(dom["name"])
-    roof["timing"] = ("CUDA events around each launch on its stream, over a second region of "
-                      "the same K steps (value comes from an event-free region)")
+    dom = rl["instances"][0]
+    roof = {"bound": dom["bound"], "achieved": dom["achieved"], "peak": dom["peak_burst"],
+            "unit": dom["unit"], "frac": dom["frac_burst"], "traffic": dom["traffic"],
+            "kernel": dom["kernel"], "shape": dom["shape"],
+            "frac_burst": dom["frac_burst"], "frac_sustained": dom["frac_sustained"],
+            "peak_sustained": dom["peak_sustained"],
+            "peak_source": peaks["source"] + (" bf16 GEMM x 2 (nominal FP8/BF16 ratio); burst, "
+                                              "sustained beside it" if dom["bound"] == "tensor"
+                                              else " copy bandwidth"),
+            "per_instantiation": rl["instances"],
+            "step": {"roofline_ms": rl["roofline_ms_per_step"],
+                     "measured_ms_graph": ms_step, "measured_ms_profiled": profiled_ms_step,
+                     "frac": rl["roofline_ms_per_step"] / ms_step,
+                     "note": "sum over the step's launches of max(flops / FP8 burst peak, "
+                             "algorithmic bytes / HBM peak), against the measured step time"},
+            "timing": ("CUDA events around each launch on its stream, over a second region of "
+                       "the same K steps (value comes from an event-free region)")}
 
     # ---- end to end through the C ABI with host buffers
     e2e = run_e2e(fp, layers, cache, ws, ctx, N, dev, world, args, stream)
 
-    # ---- the MLP-level workloads (weight caching, block MLPs)
+    # ---- the other workloads: one small linear, weight caching, block MLPs
     workloads = None
     if not args.no_mlp:
         del layers
-        workloads = run_mlp_workloads(fp, dev, stream)
-        peaks_fp8 = fp8_peak
+        workloads = {"c0_linear_512_2048_tokens": run_c0(fp, dev, stream)}
+        workloads.update(run_mlp_workloads(fp, dev, stream, peaks))
         lb = workloads["large_block_mlp_4096_14336"]
-        lb["gemm_frac_of_fp8_peak"] = lb["gemm_tflops"] / peaks_fp8
+        lb["gemm_frac_of_fp8_peak_burst"] = lb["gemm_tflops"] / peaks["fp8_tflops"]
+        lb["gemm_frac_of_fp8_peak_sustained"] = lb["gemm_tflops"] / peaks["fp8_tflops_sustained"]
         workloads.update(run_plain_and_assay(fp, dev, stream))
 
-    # ---- CPU baseline (rank 0, one GPU only)
+    # ---- CPU baselines: the oracle on the host cores (rank 0, one GPU only),
+    # single-threaded and on every core, per workload
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n_s = 2048
-        tps, dt = oracle_tokens_per_s(n_s)
-        cpu = {"value": tps, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"{n_s} tokens per linear (of {N_TOKENS}), all four shapes, once; "
-                         f"{dt:.1f} s"}
+        cores = os.cpu_count() or 1
+        one = run_oracle_timing(1, {"c1_tokens": 512})
+        allc = run_oracle_timing(cores, {"c1_tokens": 512})
+        cpu = {"value": allc["c1"]["tokens_per_s"], "unit": "tokens/s", "cores": cores,
+               "kind": "oracle",
+               "sample": allc["c1"]["sample"] + f" (of {N_TOKENS}); {allc['c1']['seconds']:.1f} s",
+               "single_thread": {"value": one["c1"]["tokens_per_s"], "cores": 1,
+                                 "sample": one["c1"]["sample"]},
+               "note": "all cores: independent samples side by side on a thread pool (numpy "
+                       "releases the interpreter lock), BLAS on all cores; single thread: one "
+                       "sample, BLAS on one thread"}
+        if workloads is not None:
+            workloads["cpu_baseline_per_workload"] = {"single_thread": one, "all_cores": allc}
 
     pages_tps = tokens_per_step / (sum(PAGES_FUSED_MS) / 1e3)
     if rank == 0:
@@ -415,7 +603,9 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak",
             "vs_baseline": value / pages_tps,
             "dtype": "fp8 (e4m3/e5m2) x fp8 -> f32 accumulate -> bf16",
-            "data": "synthetic (seeded normal bf16: X~N(0,1), W~N(0,0.02), dY~N(0,1e-3))",
+            "data": "synthetic (seeded normal bf16 drawn on the host: X~N(0,1), W~N(0,0.02), "
+                    "dY~N(0,1e-3))",
+            "input_sha256": hashes,
             "config": {"workload": "isolated FP8 linear fwd+bwd, N=131072 tokens, shapes "
                                    "512->512/512->2048/2048->512/512->8192, tensorwise current "
                                    "scaling, fused dual-layout casts, weight quantized every step",
@@ -452,9 +642,10 @@ def run_ours(args):
     return 0
 
 
-def _traffic_for(name):
+def _traffic_for(name, shape=None):
     """DRAM bytes per launch from a committed ncu summary, when it still
-    matches the current kernel sources."""
+    matches the current kernel sources (keyed by kernel name and, where the
+    summary has it, launch shape "MxNxK")."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -468,12 +659,106 @@ def _traffic_for(name):
                 h.update(f.read())
         if d.get("csrc_sha256") != h.hexdigest():
             return None
-        return d.get("kernels", {}).get(name, {}).get("dram_bytes_per_launch")
+        ks = d.get("kernels", {})
+        if shape is not None:
+            key = f"{name} {shape[0]}x{shape[1]}x{shape[2]}"
+            if key in ks:
+                return ks[key].get("dram_bytes_per_launch")
+        return ks.get(name, {}).get("dram_bytes_per_launch")
     except (OSError, ValueError, KeyError):
         return None
 
 
-def run_mlp_workloads(fp, dev, stream):
+def run_c0(fp, dev, stream):
+    """One FP8 linear 512->512 at N = 2048 tokens, tensorwise (the smallest
+    workload): fwd + bwd time per call in 5 groups of 25 calls (median of the
+    group medians, min and max), eager launches and CUDA-graph replays, the
+    cold first call, and the outputs against the CPU oracle on the same
+    inputs (relative Frobenius error per output)."""
+    import numpy as np
+    import torch
+    import oracle as o
+    from fp8_mixed_precision_gb300 import synthetic as syn
+    N, K, O = 2048, 512, 512
+    x, w, dy = syn.linear_inputs(N, K, O, device=dev)
+    cache = fp.WeightCache()
+    h = cache.register(w, "tensorwise")
+    ws = fp.linear_workspace("tensorwise", N, K, O, dev)
+    ctx = fp.LinearContext(fp._empty_bytes(fp._ctx_bytes("tensorwise", N, K), dev), N, K)
+    y = torch.empty((N, O), dtype=torch.bfloat16, device=dev)
+    dx = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    dw = torch.empty((O, K), dtype=torch.bfloat16, device=dev)
+    ver = [0]
+
+    def step():
+        cache.begin_cycle()
+        ver[0] += 1
+        cache.get(h, ver[0], True)
+        fp.fp8_linear_fwd(x, cache, h, "tensorwise", ws=ws, y=y, ctx=ctx)
+        fp.fp8_linear_bwd(dy, ctx, cache, h, "tensorwise", ws=ws, dx=dx, dw=dw)
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    first_us = 1e3 * e0.elapsed_time(e1)
+    n_l = fp.fp8_launch_count()
+    step()
+    torch.cuda.synchronize()
+    launches = fp.fp8_launch_count() - n_l
+
+    def groups(fn):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        med = []
+        for _ in range(5):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(26)]
+            ev[0].record(stream)
+            for i in range(25):
+                fn()
+                ev[i + 1].record(stream)
+            torch.cuda.synchronize()
+            med.append(statistics.median(1e3 * ev[i].elapsed_time(ev[i + 1]) for i in range(25)))
+        return {"us_median": statistics.median(med), "us_min": min(med), "us_max": max(med),
+                "group_medians_us": med}
+
+    eager = groups(step)
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        step()
+    graph = groups(g.replay)
+    del g
+    step()
+    torch.cuda.synchronize()
+    r = o.linear_fwd_bwd(syn.bits(x), syn.bits(w), syn.bits(dy), "tensorwise")
+    rel = {}
+    for name, got in (("y", y), ("dx", dx), ("dw", dw)):
+        gg = o.bf16_to_f32(syn.bits(got)).astype(np.float64)
+        ee = o.bf16_to_f32(r[name]).astype(np.float64)
+        rel[name] = float(np.linalg.norm(gg - ee) / max(np.linalg.norm(ee), 1e-30))
+    flops = 6.0 * N * K * O
+    return {"workload": "one FP8 linear 512->512, N=2048 tokens, tensorwise, fwd+bwd",
+            "eager": dict(eager, tokens_per_s=N / (eager["us_median"] / 1e6),
+                          tflops=flops / (eager["us_median"] / 1e6) / 1e12),
+            "graph_replay": dict(graph, tokens_per_s=N / (graph["us_median"] / 1e6),
+                                 tflops=flops / (graph["us_median"] / 1e6) / 1e12),
+            "first_call_us": first_us, "launches_per_call": launches,
+            "vs_oracle_rel_frobenius": rel,
+            "input_sha256": {"X": syn.sha256(x), "W": syn.sha256(w), "dY": syn.sha256(dy)},
+            "timing": "5 groups x 25 calls, an event between calls on the launching stream; "
+                      "median of the group medians (inputs in L2: the workload is 4 MB)"}
+
+
+def run_mlp_workloads(fp, dev, stream, peaks):
     """The MLP-level workloads, timed with CUDA events on the launching stream:
     weight caching in an 8-layer block-scaled stack under GA = 4 (cached vs
     uncached step time, bitwise comparison of outputs and accumulated
@@ -536,6 +821,21 @@ def run_mlp_workloads(fp, dev, stream):
             gtimes[use].append(timed(graphs[use].replay, 2))
     gmed = {k: statistics.median(v) for k, v in gtimes.items()}
     del graphs
+    # where the difference goes: one eager cycle per mode with per-kernel events
+    kb = {}
+    for use in (False, True):
+        stk.step(xs, dys, use, keep_outputs=False)
+        torch.cuda.synchronize()
+        fp.fp8_profile_begin()
+        stk.step(xs, dys, use, keep_outputs=False)
+        torch.cuda.synchronize()
+        kb[use] = {k["name"]: (k["total_ms"], k["launches"]) for k in fp.fp8_profile_end()}
+    breakdown = {}
+    for name in sorted(set(kb[False]) | set(kb[True])):
+        u_ms, u_n = kb[False].get(name, (0.0, 0))
+        c_ms, c_n = kb[True].get(name, (0.0, 0))
+        breakdown[name] = {"uncached_ms": u_ms, "cached_ms": c_ms, "saved_ms": u_ms - c_ms,
+                           "uncached_launches": u_n, "cached_launches": c_n}
     # what caching skips: one weight quantization of each fc1 / fc2 shape
     # (device time of its kernels from the library's per-kernel events)
     wq = {}
@@ -564,7 +864,12 @@ def run_mlp_workloads(fp, dev, stream):
             "groups_uncached": gtimes[False], "groups_cached": gtimes[True]},
         "weight_quantize_ms": wq,
         "skipped_weight_quantize_ms_per_step": skipped,
-        "skipped_pct_of_uncached_step": 100.0 * skipped / gmed[False]}
+        "skipped_pct_of_uncached_step": 100.0 * skipped / gmed[False],
+        "kernel_breakdown_eager": breakdown,
+        "input_sha256": {"X": [syn.sha256(t) for t in xs], "dY": [syn.sha256(t) for t in dys],
+                         "W1": [syn.sha256(t) for t in stk.w1], "W2": [syn.sha256(t) for t in stk.w2]},
+        "kernel_breakdown_note": "one eager cycle per mode, library events around every launch: "
+                                 "device time per kernel name, uncached minus cached"}
     del stk, xs, dys, res, grads
     torch.cuda.empty_cache()
 
@@ -576,9 +881,17 @@ def run_mlp_workloads(fp, dev, stream):
         blk = FP8MLPStack(512, 2048, 1, 131072, "block", device=dev, fused=fused)
         blk.step([x], [dy], True, keep_outputs=False)
         ms = timed(lambda: blk.step([x], [dy], True, keep_outputs=False), 5)
+        fp.fp8_profile_begin()
+        blk.step([x], [dy], True, keep_outputs=False)
+        torch.cuda.synchronize()
+        rl = roofline_of(fp.fp8_profile_end(by_shape=True), 1, peaks)
         out["block_mlp_512_2048" + ("_fused" if fused else "")] = {
             "ms_per_step": ms, "tokens_per_s": 131072 / (ms / 1e3),
-            "tflops": 6 * 2 * 131072 * 512 * 2048 / (ms / 1e3) / 1e12}
+            "tflops": 6 * 2 * 131072 * 512 * 2048 / (ms / 1e3) / 1e12,
+            "roofline_ms_per_step": rl["roofline_ms_per_step"],
+            "per_instantiation": rl["instances"],
+            "input_sha256": {"X": syn.sha256(x), "dY": syn.sha256(dy),
+                             "W1": syn.sha256(blk.w1[0]), "W2": syn.sha256(blk.w2[0])}}
         del blk
         torch.cuda.empty_cache()
     del x, dy
@@ -589,15 +902,29 @@ def run_mlp_workloads(fp, dev, stream):
     dy = syn.bf16_normal((16384, 4096), 1e-3, syn.SEED_DY, device=dev)
     big.step([x], [dy], True, keep_outputs=False)
     torch.cuda.synchronize()
+    ms_clean = timed(lambda: big.step([x], [dy], True, keep_outputs=False), 3)
     fp.fp8_profile_begin()
     ms = timed(lambda: big.step([x], [dy], True, keep_outputs=False), 3)
-    ks = fp.fp8_profile_end()
+    ks_shape = fp.fp8_profile_end(by_shape=True)
+    rl = roofline_of(ks_shape, 3, peaks)
+    ks = {}
+    for r in ks_shape:
+        a = ks.setdefault(r["name"], dict(name=r["name"], launches=0, total_ms=0.0, bytes=0.0,
+                                          flops=0.0))
+        for key in ("launches", "total_ms", "bytes", "flops"):
+            a[key] += r[key]
+    ks = list(ks.values())
     gemm = [k for k in ks if k["name"].startswith("gemm_fp8")]
     g_ms = sum(k["total_ms"] for k in gemm)
     g_fl = sum(k["flops"] for k in gemm)
     out["large_block_mlp_4096_14336"] = {
         "fused_producers": True,
-        "ms_per_step": ms, "tokens_per_s": 16384 / (ms / 1e3),
+        "ms_per_step": ms_clean, "tokens_per_s": 16384 / (ms_clean / 1e3),
+        "ms_per_step_with_kernel_events": ms,
+        "roofline_ms_per_step": rl["roofline_ms_per_step"],
+        "per_instantiation": rl["instances"],
+        "input_sha256": {"X": syn.sha256(x), "dY": syn.sha256(dy),
+                         "W1": syn.sha256(big.w1[0]), "W2": syn.sha256(big.w2[0])},
         "gemm_tflops": g_fl / (g_ms / 1e3) / 1e12,
         "gemm_share": g_ms / sum(k["total_ms"] for k in ks),
         "gemm_kernels": {k["name"]: {"TFLOP/s": k["flops"] / (k["total_ms"] / 1e3) / 1e12,
@@ -821,7 +1148,11 @@ def main(argv=None):
                     help="overlap: tensorwise amax passes on a second stream")
     ap.add_argument("--no-mlp", action="store_true",
                     help="skip the MLP-level workloads reported beside the main line")
+    ap.add_argument("--oracle-timing", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
+    if args.oracle_timing is not None:     # internal: one CPU-oracle timing run (subprocess)
+        print(json.dumps(oracle_timing_worker(json.loads(args.oracle_timing))), flush=True)
+        return 0
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -227,6 +227,11 @@ fp8_status fp8_weight_cache_get(fp8_weight_cache *cache, fp8_weight_handle h, ui
                                 int use_cache, fp8_stream_t stream, int *requantized);
 
 /* ------------------------------------------------------------------ linear layer
+ * The backward policy follows the implementation paragraph of "Native FP8
+ * MLP reconstruction": the forward's rounded FP8 X and W are reused by the
+ * backward GEMMs, the incoming gradient is rounded on its own (E5M2), the
+ * scales are detached (no gradient flows through them), and every GEMM
+ * accumulates in fp32 (use_fast_accum=False) and writes BF16.
  * fp8_linear_fwd: Y[N, O] = X W^T with X quantized (E4M3, both layouts) and
  * the cached FP8 weight; writes Y (bf16) and the context the backward needs
  * (the transposed FP8 X and its scales) into `ctx`.
