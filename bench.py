@@ -570,7 +570,8 @@ def run_ours(args):
     workloads = None
     if not args.no_mlp:
         del layers
-        workloads = {"c0_linear_512_2048_tokens": run_c0(fp, dev, stream)}
+        workloads = {"c0_linear_512_2048_tokens": run_c0(fp, dev, stream),
+                     "quantizers_at_workload_shapes": run_quantizer_workloads(fp, dev, peaks)}
         workloads.update(run_mlp_workloads(fp, dev, stream, peaks))
         lb = workloads["large_block_mlp_4096_14336"]
         lb["gemm_frac_of_fp8_peak_burst"] = lb["gemm_tflops"] / peaks["fp8_tflops"]
@@ -756,6 +757,47 @@ def run_c0(fp, dev, stream):
             "input_sha256": {"X": syn.sha256(x), "W": syn.sha256(w), "dY": syn.sha256(dy)},
             "timing": "5 groups x 25 calls, an event between calls on the launching stream; "
                       "median of the group medians (inputs in L2: the workload is 4 MB)"}
+
+
+def run_quantizer_workloads(fp, dev, peaks):
+    """Every quantizer at the workloads' shapes, launched alone: 12 launches
+    per shape rotating over enough input tensors that the bytes read between
+    two uses of one input exceed L2, each launch timed by the library's
+    events.  GB/s counts algorithmic bytes (bf16 read, both FP8 layouts
+    written, scales); hbm_frac is against the measured copy bandwidth."""
+    import torch
+    from fp8_mixed_precision_gb300 import synthetic as syn
+    shapes = [("1x128", "act", 131072, 2048), ("1x128", "act", 16384, 14336),
+              ("1x128", "act", 16384, 4096), ("1x128", "act", 131072, 512),
+              ("128x128", "weight", 14336, 4096), ("128x128", "weight", 4096, 14336),
+              ("128x128", "weight", 2048, 512), ("tensorwise", "act", 131072, 8192),
+              ("tensorwise", "act", 131072, 2048)]
+    out = {}
+    for kind, role, R, C in shapes:
+        recipe = "tensorwise" if kind == "tensorwise" else "block"
+        copies = max(2, -(-(256 << 20) // (2 * R * C)))   # > 2 x L2 between reuses
+        xs = [syn.bf16_normal((R, C), 1.0, 70 + i, device=dev) for i in range(min(copies, 96))]
+        fp.fp8_quantize(xs[0], recipe, role)
+        torch.cuda.synchronize()
+        fp.fp8_profile_begin()
+        for i in range(12):
+            fp.fp8_quantize(xs[i % len(xs)], recipe, role)
+        torch.cuda.synchronize()
+        recs = fp.fp8_profile_end(by_shape=True)
+        ent = {}
+        for r in recs:
+            t = r["total_ms"] / r["launches"]
+            gbs = r["bytes"] / r["launches"] / (t / 1e3) / 1e9
+            ent[r["name"]] = {"ms_per_launch": t, "GB/s": gbs, "hbm_frac": gbs / peaks["hbm_gbs"]}
+        tot_b = sum(r["bytes"] for r in recs) / 12
+        tot_t = sum(r["total_ms"] for r in recs) / 12
+        out[f"{kind} {R}x{C}"] = {"kernels": ent, "ms": tot_t,
+                                  "GB/s": tot_b / (tot_t / 1e3) / 1e9,
+                                  "hbm_frac": tot_b / (tot_t / 1e3) / 1e9 / peaks["hbm_gbs"],
+                                  "inputs_rotated": len(xs)}
+        del xs
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_mlp_workloads(fp, dev, stream, peaks):

@@ -81,14 +81,44 @@ __device__ __forceinline__ bool any_nonfinite_bf16(uint4 a, uint4 b) {
 
 // Exact-erf GELU and its derivative in fp32 (shared by the standalone GELU
 // kernels and the fused GELU + quantize path, so both round identically).
-// Phi(h) via erfc keeps full relative precision for large negative h.
+//   GELU(h) = h Phi(h),  GELU'(h) = Phi(h) + h phi(h),
+//   Phi(h) = erfc(-h / sqrt 2) / 2,  phi(h) = exp(-h^2 / 2) / sqrt(2 pi).
+// With z = |h| / sqrt 2: erfc(z) = exp(-z^2) erfcx(z), and erfcx(z) is
+// approximated as t Q(t), t = 1 / (1 + z/2), Q the degree-7 polynomial that
+// gelu_fit.py fits (relative error 3e-6 for all z >= 0).  Phi(h) is then
+// erfc(z)/2 for h < 0 and 1 - erfc(z)/2 for h >= 0, with full relative
+// precision in the negative tail, and exp(-z^2) serves phi as well.  The
+// exponential is taken as 2^64 exp(-z^2) (normal down to the smallest
+// results bf16 can hold) and the product is scaled by 2^-64 last, so tiny
+// results round once, subnormals included.  Every finite bf16 input lands
+// within 1 bf16 ulp of the exact value (tested over all of them).
+__device__ __forceinline__ void gelu_parts(float h, float &tq, float &e64) {
+  const float z = fabsf(h) * 0.70710678118654752f;
+  const float t = __frcp_rn(fmaf(0.5f, z, 1.0f));
+  float q = 0.050986580550670624f;
+  q = fmaf(q, t, -0.11058920621871948f);
+  q = fmaf(q, t, -0.040473274886608124f);
+  q = fmaf(q, t, 0.12493661046028137f);
+  q = fmaf(q, t, 0.1622200757265091f);
+  q = fmaf(q, t, 0.24883142113685608f);
+  q = fmaf(q, t, 0.28199517726898193f);
+  q = fmaf(q, t, 0.2820955216884613f);
+  tq = t * q;                                                      // ~ erfcx(z)
+  e64 = exp2f(fmaf(-z * z, 1.4426950408889634f, 64.0f));            // 2^64 exp(-z^2)
+}
 __device__ __forceinline__ float gelu_f(float h) {
-  return 0.5f * h * erfcf(-h * 0.70710678118654752f);
+  float tq, e64;
+  gelu_parts(h, tq, e64);
+  const float hq = (0.5f * h * tq) * e64 * 5.42101086242752217e-20f;  // h erfc(z) / 2
+  return h >= 0.0f ? h - hq : hq;
 }
 __device__ __forceinline__ float gelu_grad_f(float h) {
-  const float cdf = 0.5f * erfcf(-h * 0.70710678118654752f);
-  const float pdf = expf(-0.5f * h * h) * 0.39894228040143268f;
-  return fmaf(h, pdf, cdf);
+  float tq, e64;
+  gelu_parts(h, tq, e64);
+  // h >= 0: 1 - erfc(z)/2 + h phi(h);  h < 0: erfc(z)/2 + h phi(h)
+  const float v = fmaf(h >= 0.0f ? -0.5f : 0.5f, tq, h * 0.39894228040143268f) * e64 *
+                  5.42101086242752217e-20f;
+  return (h >= 0.0f ? 1.0f : 0.0f) + v;
 }
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);

@@ -198,9 +198,10 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
 // Unit u = (M tile, N tile, K split); for a CTA pair (PR) the M index is a
 // pair of 128-row tiles and CTA `rank` takes tile 2 * pair + rank (which may
 // lie past the last M tile).
-// Tiles run N-tile fastest, or (group_m > 0, single CTAs) in groups of
-// group_m M tiles, M tile fastest within a group: the CTAs running at one
-// time then share few A and B tiles, which L2 serves to all of them.
+// Tiles run N-tile fastest, or (group_m > 0) in groups of group_m M units
+// (tiles, or tile pairs for CTA pairs), M unit fastest within a group: the
+// CTAs running at one time then share few A and B tiles, which L2 serves to
+// all of them.
 template <bool PR>
 __device__ __forceinline__ void decode_unit(const GemmArgs &g, int64_t u64, uint32_t rank, int &tm,
                                             int &tn, int &kb0, int &kb1) {
@@ -210,13 +211,16 @@ __device__ __forceinline__ void decode_unit(const GemmArgs &g, int64_t u64, uint
   const uint32_t split = u % splits;
   const uint32_t t = u / splits;
   const uint32_t tiles_n = (uint32_t)g.tiles_n;
-  if (!PR && g.group_m > 0) {
+  if (g.group_m > 0) {
+    // M units: tiles, or pairs of tiles for a CTA pair
+    const uint32_t m_units = PR ? ((uint32_t)g.tiles_m + 1) / 2 : (uint32_t)g.tiles_m;
     const uint32_t gmax = (uint32_t)g.group_m;
     const uint32_t per_group = gmax * tiles_n;
     const uint32_t m0 = t / per_group * gmax;
     const uint32_t rem = t - (m0 / gmax) * per_group;
-    const uint32_t gm = min(gmax, (uint32_t)g.tiles_m - m0);  // last group may be short
-    tm = (int)(m0 + rem % gm);
+    const uint32_t gm = min(gmax, m_units - m0);  // last group may be short
+    const uint32_t mu = m0 + rem % gm;
+    tm = PR ? (int)mu * 2 + (int)rank : (int)mu;
     tn = (int)(rem / gm);
   } else {
     tm = PR ? (int)(t / tiles_n) * 2 + (int)rank : (int)(t / tiles_n);
@@ -618,11 +622,14 @@ __global__ void __launch_bounds__(Cfg<SCALING, SPLIT, BN, MH, PR>::kThreads, 1)
         if (!ok) break;
       } else if constexpr (C::kWide) {
         // Every element's scale is (row scale) x (column scale) of its K
-        // block, both read from the scale ring.  Thread = row r of the tile
-        // (TMEM lane), 64 columns colbase .. +63; the partial is read with
-        // 32x32b loads of 8 columns, two in flight per wait, the column
-        // scales as broadcast 16-byte shared loads issued meanwhile, and
-        // acc[p] holds columns 2p, 2p + 1.
+        // block, both read from the scale ring.  The partial is read with the
+        // 16x256b TMEM shape, 64 columns per load: thread (rr, cc) =
+        // (lane / 4, lane % 4) holds rows rr + 8i (i = 0..3) of the warp's
+        // 32-row quarter and columns 8k + 2cc, +1 (k = 0..7) of its 64, so per
+        // K block it needs 4 row scales and 16 column scales (8-byte shared
+        // loads, 4 distinct per warp) instead of all 64 columns' scales.
+        // acc[8i + k] is the column pair k of row i.
+        const int rr = lane >> 2, cc = lane & 3;
         uint64_t acc[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) acc[j] = 0;
@@ -630,42 +637,42 @@ __global__ void __launch_bounds__(Cfg<SCALING, SPLIT, BN, MH, PR>::kThreads, 1)
         for (int g0 = kb0; ok && g0 < kb1; g0 += kScaleGroup) {
           const uint32_t slot = ngrp % kScaleSlots;
           if (!wait_bar(&ctl->sfull[slot], (ngrp / kScaleSlots) & 1, abort)) { ok = false; break; }
-          const float *ss = scale_ring + slot * kScaleSlotFloats;
+          const float *srow = scale_ring + slot * kScaleSlotFloats + q * 32 + rr;
+          const float *scol = scale_ring + slot * kScaleSlotFloats + BM + h * 64 + 2 * cc;
 #pragma unroll 1
           for (int kk = 0; kk < kScaleGroup; ++kk) {
             if (g0 + kk >= kb1) break;
             const uint32_t ab = nacc % NB, aph = (nacc / NB) & 1;
-            if (!wait_bar(&ctl->acc_full[ab], aph, abort)) { ok = false; break; }
+            if (!wait_bar<PR>(&ctl->acc_full[ab], aph, abort)) { ok = false; break; }
             ptx::tc_fence_after();
-            const float sa = ss[kk * kScaleRowStride + r];
-            const uint64_t sa2 = pk(sa, sa);
-            const float4 *sc4 =
-                reinterpret_cast<const float4 *>(ss + kk * kScaleRowStride + BM + h * 64);
-            // two halves of 32 columns: two 16-column TMEM loads in flight per
-            // wait, the halves' 32 column scales loaded from shared memory
-            // (broadcast 16-byte loads) and multiplied by the row scale meanwhile
+            uint64_t sb[8];  // column-scale pairs of this thread's 8 column pairs
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
+            for (int k = 0; k < 8; ++k) {
+              const float2 b2 = *reinterpret_cast<const float2 *>(scol + kk * kScaleRowStride + 8 * k);
+              sb[k] = pk(b2.x, b2.y);
+            }
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {  // TMEM lanes q*32 + 16 hb .. +15: rows rr + 8i, i = 2hb, 2hb+1
               uint32_t raw[32];
-              ptx::tmem_ld16(tl + ab * BN + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(raw));
-              ptx::tmem_ld16(tl + ab * BN + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(raw + 16));
-              uint64_t sc[16];  // row scale x column scale, column pairs 32 hf + 2 p, +1
-#pragma unroll
-              for (int v = 0; v < 8; ++v) {
-                const float4 b = sc4[8 * hf + v];
-                sc[2 * v] = mul2(sa2, pk(b.x, b.y));
-                sc[2 * v + 1] = mul2(sa2, pk(b.z, b.w));
-              }
+              ptx::tmem_ld16x256b_x8(tl + ((uint32_t)(16 * hb) << 16) + ab * BN, raw);
+              const float sa0 = srow[kk * kScaleRowStride + 16 * hb];
+              const float sa1 = srow[kk * kScaleRowStride + 16 * hb + 8];
               ptx::tmem_ld_wait();
-              if (hf == 1) {  // the partial is in registers: free the TMEM buffer
+              if (hb == 1) {  // the partial is in registers: free the TMEM buffer
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) release_acc(ab);
               }
 #pragma unroll
-              for (int p = 0; p < 16; ++p)
-                acc[16 * hf + p] = fma2(pk(__uint_as_float(raw[2 * p]), __uint_as_float(raw[2 * p + 1])),
-                                        sc[p], acc[16 * hf + p]);
+              for (int ii = 0; ii < 2; ++ii) {
+                const uint64_t sa2 = ii ? pk(sa1, sa1) : pk(sa0, sa0);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                  uint64_t &a = acc[8 * (2 * hb + ii) + k];
+                  a = fma2(pk(__uint_as_float(raw[4 * k + 2 * ii]), __uint_as_float(raw[4 * k + 2 * ii + 1])),
+                           mul2(sa2, sb[k]), a);
+                }
+              }
             }
             ++nacc;
           }
@@ -674,35 +681,25 @@ __global__ void __launch_bounds__(Cfg<SCALING, SPLIT, BN, MH, PR>::kThreads, 1)
           ++ngrp;
         }
         if (!ok) break;
-        // results straight from registers (once per tile): row m, columns
-        // colbase .. +63 (N is a multiple of 16, so a 16-column group lies
-        // wholly inside or outside C)
-        if (m < g.M) {
+        // results straight from registers (once per tile): rows
+        // slab_y0 + rr + 8i, columns colbase + 8k + 2cc and +1 (N is a multiple
+        // of 16, so n < N covers n + 1)
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int64_t n = colbase + 16 * c;
+        for (int i = 0; i < 4; ++i) {
+          const int64_t mm = slab_y0 + rr + 8 * i;
+          if (mm >= g.M) continue;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int64_t n = colbase + 8 * k + 2 * cc;
             if (n >= g.N) continue;
+            float x, y;
+            upk(acc[8 * i + k], x, y);
             if constexpr (SPLIT) {
-              float *dst = static_cast<float *>(g.out) + ((int64_t)split * g.M + m) * g.N + n;
-#pragma unroll
-              for (int p = 0; p < 8; p += 2) {
-                float x0, y0, x1, y1;
-                upk(acc[8 * c + p], x0, y0);
-                upk(acc[8 * c + p + 1], x1, y1);
-                reinterpret_cast<float4 *>(dst)[p / 2] = make_float4(x0, y0, x1, y1);
-              }
+              *reinterpret_cast<float2 *>(static_cast<float *>(g.out) +
+                                          ((int64_t)split * g.M + mm) * g.N + n) = make_float2(x, y);
             } else {
-              uint32_t w[8];
-#pragma unroll
-              for (int p = 0; p < 8; ++p) {
-                float x, y;
-                upk(acc[8 * c + p], x, y);
-                __nv_bfloat162 b = __floats2bfloat162_rn(x, y);
-                w[p] = *reinterpret_cast<uint32_t *>(&b);
-              }
-              uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(g.out) + m * g.N + n);
-              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+              *reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(g.out) + mm * g.N + n) =
+                  __floats2bfloat162_rn(x, y);
             }
           }
         }

@@ -40,10 +40,11 @@ def assert_f32_equal(got: torch.Tensor, exp: np.ndarray, what: str):
 
 
 def bf16_ulp(v: np.ndarray) -> np.ndarray:
-    """Spacing of bf16 numbers at |v| (the subnormal spacing below 2^-126)."""
+    """Spacing of bf16 numbers at |v| (the subnormal spacing 2^-133 below
+    2^-126, zero included)."""
     a = np.abs(v.astype(np.float64))
     _, ex = np.frexp(a)
-    e = np.maximum(ex.astype(np.int64) - 1, -126)
+    e = np.where(a == 0, -126, np.maximum(ex.astype(np.int64) - 1, -126))
     return np.ldexp(1.0, (e - 7).astype(np.int32))
 
 

@@ -7,7 +7,7 @@ import torch
 
 import oracle as o
 from fp8_mixed_precision_gb300 import synthetic as syn
-from parity import assert_bytes_equal, assert_f32_equal, check_gemm, to_np
+from parity import bf16_ulp, assert_bytes_equal, assert_f32_equal, check_gemm, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -119,6 +119,31 @@ def test_gelu_and_accumulate(fp):
         exp = o.grad_accumulate(exp, db)
     torch.cuda.synchronize()
     assert np.array_equal(to_np(acc).view(np.uint32), exp.view(np.uint32))
+
+
+def test_gelu_every_bf16_value(fp):
+    """GELU forward and backward on every finite bf16 value (the whole input
+    domain of the bf16 stage): within 1 bf16 ulp of the fp64 oracle.  The
+    backward runs with dA = 1 (dH is then GELU'(H) rounded once) and with a
+    seeded random dA."""
+    allb = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    fin = np.isfinite(o.bf16_to_f32(allb))
+    hb = allb[fin].reshape(-1, 128)     # 65280 finite patterns (256 are inf or NaN)
+    h = syn.from_bits(hb, "cuda")
+    ones = syn.from_bits(np.full(hb.shape, 0x3F80, np.uint16), "cuda")
+    dab = syn.bits(syn.bf16_normal(hb.shape, 1e-3, 13))
+    a = fp.fp8_gelu_fwd(h)
+    d1 = fp.fp8_gelu_bwd(ones, h)
+    d2 = fp.fp8_gelu_bwd(syn.from_bits(dab, "cuda"), h)
+    torch.cuda.synchronize()
+    for got, exp, nm in ((a, o.gelu_fwd(hb), "GELU"),
+                         (d1, o.gelu_bwd(np.full(hb.shape, 0x3F80, np.uint16), hb), "GELU'"),
+                         (d2, o.gelu_bwd(dab, hb), "dA GELU'")):
+        g = o.bf16_to_f32(to_np(got)).astype(np.float64)
+        e = o.bf16_to_f32(exp).astype(np.float64)
+        bad = ~(np.abs(g - e) <= bf16_ulp(e))
+        assert not bad.any(), (f"{nm}: {int(bad.sum())} inputs beyond 1 bf16 ulp, first "
+                               f"{hb.reshape(-1)[np.argmax(bad.reshape(-1))]:#06x}")
 
 
 def test_bounded_wait_reports_timeout_and_context_survives(fp):

@@ -14,18 +14,6 @@ from parity import assert_bytes_equal, assert_f32_equal, bf16_ulp, check_gemm, t
 
 pytestmark = pytest.mark.gpu
 
-REL_TOL = 2e-3   # relative Frobenius bound of one GEMM stage fed by exact (synthetic) inputs
-
-
-def chain_tol(stages: int) -> float:
-    """Bound for an output `stages` GEMMs away from the synthetic inputs.
-    Every stage after the first re-quantizes a bf16 input that is itself only
-    tolerance-matched to the oracle's, so a few FP8 codes (or a block scale)
-    may round differently; each stage adds at most its own 2e-3 to the
-    relative error it receives."""
-    return REL_TOL * stages
-
-
 @pytest.fixture(scope="module")
 def fp():
     from fp8_mixed_precision_gb300 import build
@@ -67,9 +55,58 @@ def _oracle_stack(xb, w1b, w2b, dyb, recipe):
     return dict(y=y, dx=g, dw1=dw1, dw2=dw2, h0=saved[0][0]["y"], xq0=saved[0][0]["xq"])
 
 
+def _stage_fwd(got, a_bits, wq, recipe, K, what):
+    """One linear's forward as a stage: the oracle quantizes the GPU's own
+    bf16 input and multiplies it with the oracle's FP8 weight; the GPU's
+    output must be within the single-GEMM bound.  Returns the oracle's
+    forward context for the backward stage."""
+    f = o.linear_fwd(a_bits, wq, recipe)
+    xq = f["xq"]
+    A = o.dequantize(xq["row"], xq["row_scale_inv"], "e4m3")
+    B = o.dequantize(wq["row"], wq["row_scale_inv"], "e4m3")
+    check_gemm(got, A @ B.T, np.abs(A) @ np.abs(B).T, K, what)
+    return f
+
+
+def _stage_bwd(dx_got, dw_got, g_bits, ctx, wq, recipe, O, N, what):
+    """One linear's backward as a stage, from the GPU's own incoming bf16
+    gradient: dgrad and wgrad within the single-GEMM bound."""
+    gq = o.quantize(g_bits, recipe, "grad")
+    A = o.dequantize(gq["row"], gq["row_scale_inv"], "e5m2")
+    B = o.dequantize(wq["col"], wq["col_scale_inv"], "e4m3")
+    check_gemm(dx_got, A @ B.T, np.abs(A) @ np.abs(B).T, O, what + " dgrad")
+    A = o.dequantize(gq["col"], gq["col_scale_inv"], "e5m2")
+    xq = ctx["xq"]
+    B = o.dequantize(xq["col"], xq["col_scale_inv"], "e4m3")
+    check_gemm(dw_got, A @ B.T, np.abs(A) @ np.abs(B).T, N, what + " wgrad")
+
+
+def _within_ulp(got, exp_bits, what):
+    g = o.bf16_to_f32(to_np(got)).astype(np.float64)
+    e = o.bf16_to_f32(exp_bits).astype(np.float64)
+    bad = ~(np.abs(g - e) <= bf16_ulp(e))
+    assert not bad.any(), f"{what}: {int(bad.sum())} entries beyond 1 bf16 ulp"
+
+
+# End-to-end sanity bound for outputs several re-quantized stages away from
+# the synthetic inputs.  Two evaluations of the same FP8 chain that differ
+# only by 1 bf16 ulp in a few GELU outputs re-quantize later tensors onto
+# different codes and block scales (E5M2 gradients keep 2 mantissa bits), so
+# their end-to-end results differ by a few percent at four stages, while the
+# FP8 chain itself is about 10% away from unquantized arithmetic.  Every
+# stage is held to the exact bounds separately (stage-wise checks); this
+# bound only catches gross errors.
+E2E_TOL = 5e-2
+
+
 @pytest.mark.parametrize("recipe", ["block", "tensorwise"])
 @pytest.mark.parametrize("N", [4096, 400])
 def test_mlp_block_parity(fp, recipe, N):
+    """One MLP block fwd + bwd, every stage against the oracle fed the GPU's
+    own inputs for that stage: both linears' forward, dgrad and wgrad within
+    the single-GEMM bound, both GELU stages within 1 bf16 ulp, the saved
+    FP8 input bytes exact; end-to-end outputs against the oracle's chain
+    within the sanity bound."""
     from fp8_mixed_precision_gb300.mlp import FP8MLPStack
     d, ffn = 512, 2048
     st = FP8MLPStack(d, ffn, 1, N, recipe)
@@ -78,23 +115,25 @@ def test_mlp_block_parity(fp, recipe, N):
     st.step([x], [dy], use_cache=True)
     torch.cuda.synchronize()
     assert fp.fp8_get_device_status() == 0
-    r = _oracle_stack(syn.bits(x), [syn.bits(st.w1[0])], [syn.bits(st.w2[0])], syn.bits(dy), recipe)
-    # first stage from synthetic inputs: bytes exact, fc1 output within the GEMM bound
-    xq_col = st.ctx1[0].ctx[:N * d].view(d, N)
-    assert_bytes_equal(xq_col, r["xq0"]["col"], "Xq colwise (fc1 context)")
-    xq = r["xq0"]
+    xb, dyb = syn.bits(x), syn.bits(dy)
+    Hb, Ab, dAb, dHb = syn.bits(st.H[0]), syn.bits(st.A[0]), syn.bits(st.dA), syn.bits(st.dH)
     w1q = o.quantize(syn.bits(st.w1[0]), recipe, "weight")
-    A = o.dequantize(xq["row"], xq["row_scale_inv"], "e4m3")
-    B = o.dequantize(w1q["row"], w1q["row_scale_inv"], "e4m3")
-    check_gemm(st.H[0], A @ B.T, np.abs(A) @ np.abs(B).T, d, "H = fc1(X)")
-    # end to end (later stages see tolerance-matched inputs): relative Frobenius
-    # GEMM stages on the longest path from the synthetic inputs: Y = fc2(GELU(fc1 X)) 2;
-    # dX = fc1 dgrad of GELU'(fc1 X) * fc2 dgrad(dY) 2; dW1 = fc1 wgrad of that 3; dW2 2
-    rels = {"Y": (_rel(st.Y[0], r["y"]), 2), "dX": (_rel(st.g[0], r["dx"]), 2),
-            "dW1": (_rel(st.dw1[0], o.bf16_to_f32(r["dw1"][0])), 3),
-            "dW2": (_rel(st.dw2[0], o.bf16_to_f32(r["dw2"][0])), 2)}
-    for k, (v, n) in rels.items():
-        assert v <= chain_tol(n), f"{k}: relative Frobenius error {v:.3g} ({n} stages)"
+    w2q = o.quantize(syn.bits(st.w2[0]), recipe, "weight")
+    f1 = _stage_fwd(st.H[0], xb, w1q, recipe, d, "fc1 fprop")
+    xq_col = st.ctx1[0].ctx[:N * d].view(d, N)
+    assert_bytes_equal(xq_col, f1["xq"]["col"], "Xq colwise (fc1 context)")
+    _within_ulp(st.A[0], o.gelu_fwd(Hb), "A = GELU(H)")
+    f2 = _stage_fwd(st.Y[0], Ab, w2q, recipe, ffn, "fc2 fprop")
+    _stage_bwd(st.dA, st.dwb2, dyb, f2, w2q, recipe, d, N, "fc2")
+    _within_ulp(st.dH, o.gelu_bwd(dAb, Hb), "dH = dA GELU'(H)")
+    _stage_bwd(st.g[0], st.dwb1, dHb, f1, w1q, recipe, ffn, N, "fc1")
+    # end to end against the oracle's own chain: sanity bound only
+    r = _oracle_stack(xb, [syn.bits(st.w1[0])], [syn.bits(st.w2[0])], dyb, recipe)
+    rels = {"Y": _rel(st.Y[0], r["y"]), "dX": _rel(st.g[0], r["dx"]),
+            "dW1": _rel(st.dw1[0], o.bf16_to_f32(r["dw1"][0])),
+            "dW2": _rel(st.dw2[0], o.bf16_to_f32(r["dw2"][0]))}
+    for k, v in rels.items():
+        assert v <= E2E_TOL, f"{k}: end-to-end relative Frobenius error {v:.3g}"
 
 
 @pytest.mark.parametrize("recipe", ["block", "tensorwise"])
@@ -123,7 +162,16 @@ def test_stack_weight_cache_bitwise(fp, recipe):
             assert torch.equal(dx1.view(torch.int16), dx2.view(torch.int16))
     for a, b in zip(g_u, g_c):
         assert torch.equal(a.view(torch.int32), b.view(torch.int32))
-    # and the accumulated gradients agree with the oracle's chain + fp32 accumulation
+    # the last stage of the last microbatch against the oracle fed the GPU's
+    # own inputs: layer 0's fc1 wgrad from its dH and that microbatch's X
+    w1q0 = o.quantize(syn.bits(st.w1[0]), recipe, "weight")
+    f1 = o.linear_fwd(syn.bits(xs[-1]), w1q0, recipe)
+    gq = o.quantize(syn.bits(st.dH), recipe, "grad")
+    A = o.dequantize(gq["col"], gq["col_scale_inv"], "e5m2")
+    B = o.dequantize(f1["xq"]["col"], f1["xq"]["col_scale_inv"], "e4m3")
+    check_gemm(st.dwb1, A @ B.T, np.abs(A) @ np.abs(B).T, N, "layer 0 fc1 wgrad, last microbatch")
+    # the accumulated gradients against the oracle's chain + fp32
+    # accumulation: end-to-end sanity bound (see E2E_TOL)
     w1b = [syn.bits(w) for w in st.w1]      # the stack's synthetic weights (generator output)
     w2b = [syn.bits(w) for w in st.w2]
     acc1 = [np.zeros((ffn, d), np.float32) for _ in range(L)]
@@ -132,11 +180,8 @@ def test_stack_weight_cache_bitwise(fp, recipe):
         for l in range(L):
             acc1[l] = o.grad_accumulate(acc1[l], r["dw1"][l])
     for l in range(L):
-        # dW1[l]: 2 (L - 1 - l) dgrads through the later blocks, fc2(l) dgrad,
-        # then the wgrad -> 2 (L - l) stages
         rel = _rel(g_c[l], acc1[l])
-        n = 2 * (L - l)
-        assert rel <= chain_tol(n), f"dW1[{l}] accumulated: relative Frobenius error {rel:.3g}"
+        assert rel <= E2E_TOL, f"dW1[{l}] accumulated: end-to-end relative Frobenius error {rel:.3g}"
 
 
 @pytest.mark.parametrize("K,O", [(4096, 14336), (14336, 4096)])
