@@ -1237,7 +1237,12 @@ cudaError_t launch_gemm(const uint8_t *A, int a_fmt, const float *a_sinv, const 
   // tiles' A and B blocks shared through L2.  Other GEMMs keep the N-tile
   // fastest order (measured faster for the K = 512 shapes, whose output
   // rows are then written across all N tiles at once).
-  g.group_m = (scaling == FP8_SCALING_1x128_1x128 && p.bn == kWideBN) ? std::min(16, p.tiles_m) : 0;
+  // Deep-K 1x128 x 128x128 GEMMs (fprop/dgrad, K >= 2048) gain the same way
+  // (16384 x 14336 x 4096: 0.82 -> 0.78 ms).
+  g.group_m = ((scaling == FP8_SCALING_1x128_1x128 && p.bn == kWideBN) ||
+               (scaling == FP8_SCALING_1x128_128x128 && p.kbs >= 16))
+                  ? std::min(16, p.tiles_m)
+                  : 0;
   const bool split = p.splits > 1;
   cudaError_t e;
   switch (scaling) {
