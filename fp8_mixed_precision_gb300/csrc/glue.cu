@@ -11,7 +11,7 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// gelu_f / gelu_grad_f / pack_bf16x2 live in common.cuh (shared with the
+// gelu_f2 / gelu_grad_f2 / pack_bf16x2 live in common.cuh (shared with the
 // fused GELU + quantize path).
 
 __global__ void gelu_fwd_kernel(const uint4 *__restrict__ H, uint4 *__restrict__ A, int64_t n8) {
@@ -21,7 +21,11 @@ __global__ void gelu_fwd_kernel(const uint4 *__restrict__ H, uint4 *__restrict__
     const uint32_t w[4] = {h.x, h.y, h.z, h.w};
     uint32_t o[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) o[k] = pack_bf16x2(gelu_f(bf16lo(w[k])), gelu_f(bf16hi(w[k])));
+    for (int k = 0; k < 4; ++k) {
+      float g0, g1;
+      gelu_f2(bf16lo(w[k]), bf16hi(w[k]), g0, g1);
+      o[k] = pack_bf16x2(g0, g1);
+    }
     A[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
@@ -34,9 +38,11 @@ __global__ void gelu_bwd_kernel(const uint4 *__restrict__ dA, const uint4 *__res
     const uint32_t hw[4] = {h.x, h.y, h.z, h.w}, dw[4] = {d.x, d.y, d.z, d.w};
     uint32_t o[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      o[k] = pack_bf16x2(__fmul_rn(bf16lo(dw[k]), gelu_grad_f(bf16lo(hw[k]))),
-                       __fmul_rn(bf16hi(dw[k]), gelu_grad_f(bf16hi(hw[k]))));
+    for (int k = 0; k < 4; ++k) {
+      float g0, g1;
+      gelu_grad_f2(bf16lo(hw[k]), bf16hi(hw[k]), g0, g1);
+      o[k] = pack_bf16x2(__fmul_rn(bf16lo(dw[k]), g0), __fmul_rn(bf16hi(dw[k]), g1));
+    }
     dH[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }

@@ -312,14 +312,20 @@ __global__ void __launch_bounds__(kQThreads, 2)
         uint32_t o4[4];
         if (PRE == 1) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) o4[j] = pack_bf16x2(gelu_f(bf16lo(wi[j])), gelu_f(bf16hi(wi[j])));
+          for (int j = 0; j < 4; ++j) {
+            float g0, g1;
+            gelu_f2(bf16lo(wi[j]), bf16hi(wi[j]), g0, g1);
+            o4[j] = pack_bf16x2(g0, g1);
+          }
         } else {
           const uint4 hw = *reinterpret_cast<const uint4 *>(&S.in[1][(rr + 16 * i) * 128 + 8 * cg]);
           const uint32_t hi4[4] = {hw.x, hw.y, hw.z, hw.w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            o4[j] = pack_bf16x2(__fmul_rn(bf16lo(wi[j]), gelu_grad_f(bf16lo(hi4[j]))),
-                                __fmul_rn(bf16hi(wi[j]), gelu_grad_f(bf16hi(hi4[j]))));
+          for (int j = 0; j < 4; ++j) {
+            float g0, g1;
+            gelu_grad_f2(bf16lo(hi4[j]), bf16hi(hi4[j]), g0, g1);
+            o4[j] = pack_bf16x2(__fmul_rn(bf16lo(wi[j]), g0), __fmul_rn(bf16hi(wi[j]), g1));
+          }
         }
         xw[i] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
       }

@@ -5,6 +5,7 @@ single launches (e.g. under ncu) and timing them with CUDA events.
         --scaling tensor --reps 3
     python -m fp8_mixed_precision_gb300.kernel_case quantize --M 131072 --N 2048 \
         --recipe tensorwise --role act --reps 3
+    python -m fp8_mixed_precision_gb300.kernel_case gelu_bwd --M 131072 --N 2048 --reps 7
 """
 from __future__ import annotations
 
@@ -19,7 +20,7 @@ from fp8_mixed_precision_gb300 import synthetic as syn
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("kind", choices=["gemm", "quantize", "gelu"])
+    ap.add_argument("kind", choices=["gemm", "quantize", "gelu", "gelu_bwd"])
     ap.add_argument("--M", type=int, required=True)
     ap.add_argument("--N", type=int, required=True)
     ap.add_argument("--K", type=int, default=512)
@@ -57,12 +58,19 @@ def main(argv=None):
         run = lambda: fp.fp8_quantize(x, a.recipe, a.role)
         flops = 0.0
         nbytes = (6.0 if a.recipe == "tensorwise" else 4.125) * a.M * a.N
-    else:
+    elif a.kind == "gelu":
         h = syn.bf16_normal((a.M, a.N), 1.0, 4, device=dev)
         out = torch.empty_like(h)
         run = lambda: fp.fp8_gelu_fwd(h, out=out)
         flops = 0.0
         nbytes = 4.0 * a.M * a.N
+    else:
+        h = syn.bf16_normal((a.M, a.N), 1.0, 4, device=dev)
+        da = syn.bf16_normal((a.M, a.N), 1.0, 5, device=dev)
+        out = torch.empty_like(h)
+        run = lambda: fp.fp8_gelu_bwd(da, h, out=out)
+        flops = 0.0
+        nbytes = 6.0 * a.M * a.N
     run()
     torch.cuda.synchronize()
     ts = []
