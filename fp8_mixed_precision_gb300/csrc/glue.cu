@@ -1,7 +1,7 @@
 // MLP glue around the FP8 linears: exact-erf GELU forward/backward (fp32
 // arithmetic, bf16 in/out) and fp32 gradient accumulation over microbatches.
-// Elementwise and HBM-bound: 16-byte vector loads/stores, grid-stride over a
-// grid sized in multiples of the SM count.
+// Elementwise: 16-byte vector loads/stores, grid-stride over a grid sized in
+// multiples of the SM count (the GELU kernels: exactly the resident blocks).
 #include "common.cuh"
 #include "internal.h"
 
@@ -14,37 +14,47 @@ constexpr int kThreads = 256;
 // gelu_f2 / gelu_grad_f2 / pack_bf16x2 live in common.cuh (shared with the
 // fused GELU + quantize path).
 
-__global__ void gelu_fwd_kernel(const uint4 *__restrict__ H, uint4 *__restrict__ A, int64_t n8) {
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const uint4 h = H[i];
-    const uint32_t w[4] = {h.x, h.y, h.z, h.w};
-    uint32_t o[4];
+__device__ __forceinline__ uint4 gelu8(uint4 h) {
+  const uint32_t w[4] = {h.x, h.y, h.z, h.w};
+  uint32_t o[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      float g0, g1;
-      gelu_f2(bf16lo(w[k]), bf16hi(w[k]), g0, g1);
-      o[k] = pack_bf16x2(g0, g1);
-    }
-    A[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  for (int k = 0; k < 4; ++k) {
+    float g0, g1;
+    gelu_f2(bf16lo(w[k]), bf16hi(w[k]), g0, g1);
+    o[k] = pack_bf16x2(g0, g1);
   }
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-__global__ void gelu_bwd_kernel(const uint4 *__restrict__ dA, const uint4 *__restrict__ H,
-                                uint4 *__restrict__ dH, int64_t n8) {
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const uint4 h = H[i], d = dA[i];
-    const uint32_t hw[4] = {h.x, h.y, h.z, h.w}, dw[4] = {d.x, d.y, d.z, d.w};
-    uint32_t o[4];
+__device__ __forceinline__ uint4 gelu_bwd8(uint4 d, uint4 h) {
+  const uint32_t hw[4] = {h.x, h.y, h.z, h.w}, dw[4] = {d.x, d.y, d.z, d.w};
+  uint32_t o[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      float g0, g1;
-      gelu_grad_f2(bf16lo(hw[k]), bf16hi(hw[k]), g0, g1);
-      o[k] = pack_bf16x2(__fmul_rn(bf16lo(dw[k]), g0), __fmul_rn(bf16hi(dw[k]), g1));
-    }
-    dH[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  for (int k = 0; k < 4; ++k) {
+    float g0, g1;
+    gelu_grad_f2(bf16lo(hw[k]), bf16hi(hw[k]), g0, g1);
+    o[k] = pack_bf16x2(__fmul_rn(bf16lo(dw[k]), g0), __fmul_rn(bf16hi(dw[k]), g1));
   }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Grid-stride over 8-element vectors on a grid of exactly the resident
+// blocks, at full occupancy (32 registers: 8 blocks of 256 threads per SM).
+// Measured on 131072 x 2048: forward 0.255 ms, backward 0.293 ms; two
+// vectors per iteration at 40-52 registers ran 0.267 / 0.314-0.339 ms.
+__global__ void __launch_bounds__(kThreads, 8) gelu_fwd_kernel(const uint4 *__restrict__ H,
+                                                               uint4 *__restrict__ A, int64_t n8) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride)
+    A[i] = gelu8(H[i]);
+}
+
+__global__ void __launch_bounds__(kThreads, 8) gelu_bwd_kernel(const uint4 *__restrict__ dA,
+                                                               const uint4 *__restrict__ H,
+                                                               uint4 *__restrict__ dH, int64_t n8) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride)
+    dH[i] = gelu_bwd8(dA[i], H[i]);
 }
 
 __global__ void grad_accumulate_kernel(float4 *__restrict__ acc, const uint2 *__restrict__ dW,
@@ -66,22 +76,44 @@ unsigned grid_for(int64_t items) {
   return (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms() * 8));
 }
 
+// Grid of the GELU kernels: every block resident at once (blocks per SM from
+// the occupancy calculator, per kernel and device), so that no block starts
+// after the others have finished their grid-stride share.
+template <typename Kernel>
+unsigned grid_resident(Kernel kernel, int64_t items, int *per_dev) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int bps = 8;
+  if (dev >= 0 && dev < 64) {
+    if (per_dev[dev] == 0) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, 0) != cudaSuccess || n < 1)
+        n = 1;
+      per_dev[dev] = n;
+    }
+    bps = per_dev[dev];
+  }
+  const int64_t want = (items + kThreads - 1) / kThreads;
+  return (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms() * bps));
+}
+int g_gelu_fwd_bps[64], g_gelu_bwd_bps[64];
+
 }  // namespace
 
 cudaError_t launch_gelu_fwd(const void *H, void *A, int64_t n, cudaStream_t st) {
   const int64_t n8 = n / 8;
   LaunchScope ls("gelu_fwd", st, 4.0 * n, 0.0, n);
-  gelu_fwd_kernel<<<grid_for(n8), kThreads, 0, st>>>(static_cast<const uint4 *>(H),
-                                                      static_cast<uint4 *>(A), n8);
+  const unsigned grid = grid_resident(gelu_fwd_kernel, n8, g_gelu_fwd_bps);
+  gelu_fwd_kernel<<<grid, kThreads, 0, st>>>(static_cast<const uint4 *>(H), static_cast<uint4 *>(A), n8);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gelu_bwd(const void *dA, const void *H, void *dH, int64_t n, cudaStream_t st) {
   const int64_t n8 = n / 8;
   LaunchScope ls("gelu_bwd", st, 6.0 * n, 0.0, n);
-  gelu_bwd_kernel<<<grid_for(n8), kThreads, 0, st>>>(static_cast<const uint4 *>(dA),
-                                                      static_cast<const uint4 *>(H),
-                                                      static_cast<uint4 *>(dH), n8);
+  const unsigned grid = grid_resident(gelu_bwd_kernel, n8, g_gelu_bwd_bps);
+  gelu_bwd_kernel<<<grid, kThreads, 0, st>>>(static_cast<const uint4 *>(dA), static_cast<const uint4 *>(H),
+                                             static_cast<uint4 *>(dH), n8);
   return cudaGetLastError();
 }
 

@@ -20,7 +20,8 @@ from fp8_mixed_precision_gb300 import synthetic as syn
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("kind", choices=["gemm", "quantize", "gelu", "gelu_bwd"])
+    ap.add_argument("kind", choices=["gemm", "quantize", "gelu", "gelu_bwd", "gelu_quant",
+                                     "gelu_bwd_quant"])
     ap.add_argument("--M", type=int, required=True)
     ap.add_argument("--N", type=int, required=True)
     ap.add_argument("--K", type=int, default=512)
@@ -64,13 +65,25 @@ def main(argv=None):
         run = lambda: fp.fp8_gelu_fwd(h, out=out)
         flops = 0.0
         nbytes = 4.0 * a.M * a.N
-    else:
+    elif a.kind == "gelu_bwd":
         h = syn.bf16_normal((a.M, a.N), 1.0, 4, device=dev)
         da = syn.bf16_normal((a.M, a.N), 1.0, 5, device=dev)
         out = torch.empty_like(h)
         run = lambda: fp.fp8_gelu_bwd(da, h, out=out)
         flops = 0.0
         nbytes = 6.0 * a.M * a.N
+    else:  # fused GELU (backward) + 1x128 quantization, both layouts
+        h = syn.bf16_normal((a.M, a.N), 1.0, 4, device=dev)
+        if a.kind == "gelu_quant":
+            q = fp.QuantizedTensor(a.M, a.N, "act", dev)
+            run = lambda: fp.fp8_gelu_quantize(h, q)
+            nbytes = 4.125 * a.M * a.N
+        else:
+            da = syn.bf16_normal((a.M, a.N), 1.0, 5, device=dev)
+            q = fp.QuantizedTensor(a.M, a.N, "grad", dev)
+            run = lambda: fp.fp8_gelu_bwd_quantize(da, h, q)
+            nbytes = 6.125 * a.M * a.N
+        flops = 0.0
     run()
     torch.cuda.synchronize()
     ts = []
