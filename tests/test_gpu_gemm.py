@@ -61,9 +61,11 @@ def test_gemm_parity(fp, M, N, K, scaling):
     _run(fp, M, N, K, scaling)
 
 
-@pytest.mark.parametrize("M,N,K", [(8192, 512, 512), (8320, 400, 496), (16384, 2048, 256)])
+@pytest.mark.parametrize("M,N,K", [(8192, 512, 512), (8320, 400, 496), (16384, 2048, 256),
+                                   (8192, 2176, 512), (4224, 8192, 384)])
 def test_gemm_short_k_many_tiles(fp, M, N, K):
-    # output-bound shapes: many M tiles over a short (ragged) K
+    # output-bound shapes: many M tiles over a short (ragged) K; 2176 = 8.5
+    # 256-wide N tiles (a half-filled last tile), 8192 x 384 a ragged M
     _run(fp, M, N, K, "tensor", "e4m3", "e4m3", seed=M + N)
 
 
