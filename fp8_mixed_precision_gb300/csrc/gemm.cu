@@ -13,8 +13,8 @@
 //                             register accumulator (software promotion).
 //
 // Structure: persistent CTAs (one per SM), warp-specialised, tile BM x BN
-// (128 x 256 when N allows; 128 x 128 for narrow outputs and for
-// 1x128 x 1x128 scaling).
+// (128 x 256 when N allows; 128 x 192 for 1x128 x 1x128 scaling of outputs
+// at least 320 wide; 128 x 128 for narrow outputs).
 //   warp 0      TMA producer: A (128 rows) and B (BN rows) tiles of 128 bytes
 //               along K, 128B swizzle, into a shared-memory ring guarded by
 //               full/empty mbarriers
@@ -23,10 +23,14 @@
 //   warps 2-9   epilogue: tcgen05.ld from TMEM, scale, round to bf16, stage
 //               32x64 slabs in 128B-swizzled shared memory, TMA bulk stores.
 //               Warp w reads TMEM lanes 32*(w%4)..+31 and column half (w-2)/4.
-//   1x128 x 1x128: warps 2-17 are the epilogue, warp w taking column quarter
-//               (w-2)/4 of lanes 32*(w%4)..+31, read with the 16x256b shape
-//               (4 rows x 8 columns per thread) and staged as unswizzled
-//               32x32 slabs.
+//   1x128 x 1x128, 128 x 128 tiles: warps 2-17 are the epilogue, warp w
+//               taking column quarter (w-2)/4 of lanes 32*(w%4)..+31, read
+//               with the 16x256b shape (4 rows x 8 columns per thread) and
+//               staged as unswizzled 32x32 slabs.
+//   1x128 x 1x128, 128 x 192 tiles: warpgroup 0 = producer, MMA issuer and
+//               two scale-loader warps; warps 4-15 the epilogue (64 columns
+//               each, 16x256b reads), results stored from registers once per
+//               tile; a register split between the warpgroups (setmaxnreg).
 // TMEM holds 512/BN accumulator buffers used round-robin, so the epilogue of
 // one tile (tensor scaling) or one K block (block scaling) overlaps the
 // following MMAs.  Deep-K tensor-scaled GEMMs use 256-row tiles (two M
@@ -95,9 +99,10 @@ constexpr int kScaleRingBytes = kScaleSlots * kScaleSlotFloats * 4 + kScaleRowSt
 //   PR  CTA pair (cluster of 2, cta_group::2 MMAs): each CTA stages its own
 //       A rows and half of the B tile.
 // Epilogue warps: 8 (two per TMEM lane quarter, each taking half of the
-// tile's columns), or 16 for the 1x128 x 1x128 promotion (four per lane
-// quarter, 32 columns each), whose per-K-block TMEM drain is latency-bound
-// and needs more warps per scheduler to overlap it.
+// tile's columns), or for the 1x128 x 1x128 promotion 16 (128-wide tiles:
+// four per lane quarter, 32 columns each) or 12 (192-wide tiles: three per
+// lane quarter, 64 columns each), whose per-K-block TMEM drain is
+// latency-bound and needs more warps per scheduler to overlap it.
 // Shared memory: operand ring, bf16 output staging (none for split-K, which
 // writes fp32 partials from registers) and the control block (the column
 // scale area only for 1x128 x 1x128).  Output slabs are 32 rows x 64 columns
