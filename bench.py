@@ -643,6 +643,23 @@ def run_ours(args):
     return 0
 
 
+def kernel_source_digest():
+    """SHA-256 over the kernel sources with comments and whitespace removed:
+    a committed ncu summary stays valid across comment-only edits and goes
+    stale on any code change."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "fp8_mixed_precision_gb300", "csrc")
+    for fn in sorted(os.listdir(d)):
+        with open(os.path.join(d, fn), encoding="utf-8") as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)   # block comments
+        src = re.sub(r"//[^\n]*", " ", src)                # line comments
+        h.update(fn.encode() + b"\0" + " ".join(src.split()).encode() + b"\0")
+    return h.hexdigest()
+
+
 def _traffic_for(name, shape=None):
     """DRAM bytes per launch from a committed ncu summary, when it still
     matches the current kernel sources (keyed by kernel name and, where the
@@ -653,12 +670,7 @@ def _traffic_for(name, shape=None):
     try:
         with open(p) as f:
             d = json.load(f)
-        import hashlib
-        h = hashlib.sha256()
-        for fn in sorted(os.listdir(os.path.join(ROOT, "fp8_mixed_precision_gb300", "csrc"))):
-            with open(os.path.join(ROOT, "fp8_mixed_precision_gb300", "csrc", fn), "rb") as f:
-                h.update(f.read())
-        if d.get("csrc_sha256") != h.hexdigest():
+        if d.get("csrc_sha256") != kernel_source_digest():
             return None
         ks = d.get("kernels", {})
         if shape is not None:
