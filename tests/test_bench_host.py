@@ -85,3 +85,24 @@ def test_reference_arm_json_line():
     assert e["value"] == d["value"] and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
     assert "workload" in d["config"]
+
+
+def test_kernel_source_digest_ignores_comments_only():
+    """The digest that keys the committed DRAM-traffic figures changes with
+    any code edit of the kernel sources and with no comment-only edit."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    import tempfile, shutil
+    with tempfile.TemporaryDirectory() as d:
+        csrc = os.path.join(d, "fp8_mixed_precision_gb300", "csrc")
+        shutil.copytree(os.path.join(ROOT, "fp8_mixed_precision_gb300", "csrc"), csrc)
+        bench.ROOT = d
+        base = bench.kernel_source_digest()
+        p = os.path.join(csrc, "glue.cu")
+        src = open(p).read()
+        open(p, "w").write("// a new comment line\n" + src.replace("\n", "  \n", 3) + "\n/* block\n comment */\n")
+        assert bench.kernel_source_digest() == base
+        open(p, "w").write(src.replace("kThreads = 256", "kThreads = 128", 1))
+        assert bench.kernel_source_digest() != base
