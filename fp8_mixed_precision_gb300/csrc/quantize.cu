@@ -29,6 +29,12 @@
 //   transpose thread t reads a 16-row x 4-column byte block (conflict-free
 //             32-bit shared loads), transposes it with byte permutes and writes
 //             4 transposed rows of 16 bytes (8 lanes = one 128-byte segment)
+// Fused producers (1x128 only): PRE = 1 applies GELU, PRE = 2 forms
+// dA * GELU'(H), to the thread's register tile right after its shared read,
+// rounding to bf16 there, so the quantizer sees exactly the bf16 tensor the
+// unfused GELU kernels would write.  PRE = 2 loads dA and H into the two
+// buffers together and refills both with the next tile as soon as every
+// thread holds its elements (after the maxima).
 // Ragged tails: the last tile may have fewer rows/columns (multiples of 16);
 // absent elements are zero-filled by the TMA load (zeros never raise an amax)
 // and never stored.  Every wait on a tile is bounded: on expiry the kernel
