@@ -740,10 +740,16 @@ fp8_status fp8_profile_end(fp8_kernel_stat *out, int cap, int *n) {
 struct fp8_host_pipeline {
   int device = 0;
   cudaStream_t copy_in = nullptr, compute = nullptr, copy_out = nullptr;
+  // Per slot, the forward and the backward halves of a step are tracked
+  // apart, so that dY streams in while the forward runs and Y streams out
+  // while the backward runs.
   struct Slot {
-    cudaEvent_t in_done = nullptr;       // this slot's inputs are on the device
-    cudaEvent_t compute_done = nullptr;  // this slot's kernels have finished
-    cudaEvent_t out_done = nullptr;      // this slot's results are on the host
+    cudaEvent_t in_fwd = nullptr;    // X and W are on the device
+    cudaEvent_t in_bwd = nullptr;    // dY is on the device
+    cudaEvent_t fwd_done = nullptr;  // the forward's kernels (the last readers of X, W) finished
+    cudaEvent_t bwd_done = nullptr;  // the backward's kernels (the last readers of dY) finished
+    cudaEvent_t out_fwd = nullptr;   // Y is on the host
+    cudaEvent_t out_bwd = nullptr;   // dX and dW are on the host
   };
   std::vector<Slot> slots;
   cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
@@ -752,7 +758,7 @@ struct fp8_host_pipeline {
 void fp8_host_pipeline_destroy(fp8_host_pipeline *p) {
   if (!p) return;
   for (auto &s : p->slots)
-    for (cudaEvent_t e : {s.in_done, s.compute_done, s.out_done})
+    for (cudaEvent_t e : {s.in_fwd, s.in_bwd, s.fwd_done, s.bwd_done, s.out_fwd, s.out_bwd})
       if (e) cudaEventDestroy(e);
   for (cudaEvent_t e : {p->fork_ev, p->join_ev})
     if (e) cudaEventDestroy(e);
@@ -771,7 +777,7 @@ fp8_status fp8_host_pipeline_create(int slots, fp8_host_pipeline **out) {
     ok = ok && cudaStreamCreateWithFlags(s, cudaStreamNonBlocking) == cudaSuccess;
   p->slots.resize((size_t)slots);
   for (auto &s : p->slots)
-    for (cudaEvent_t *e : {&s.in_done, &s.compute_done, &s.out_done})
+    for (cudaEvent_t *e : {&s.in_fwd, &s.in_bwd, &s.fwd_done, &s.bwd_done, &s.out_fwd, &s.out_bwd})
       ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
   for (cudaEvent_t *e : {&p->fork_ev, &p->join_ev})
     ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
@@ -812,35 +818,48 @@ fp8_status fp8_linear_step_host(fp8_host_pipeline *p, int slot, int64_t N,
 
   auto &s = p->slots[(size_t)slot];
   const size_t xb = (size_t)N * K * 2, wb = (size_t)O * K * 2, gb = (size_t)N * O * 2;
-  bool ok = cudaStreamWaitEvent(p->copy_in, s.compute_done, 0) == cudaSuccess &&
+  // copy-in: X and W once this slot's previous forward has read them, dY once
+  // its previous backward has
+  bool ok = cudaStreamWaitEvent(p->copy_in, s.fwd_done, 0) == cudaSuccess &&
             cudaMemcpyAsync(dev->X, host->X, xb, cudaMemcpyHostToDevice, p->copy_in) ==
                 cudaSuccess &&
             cudaMemcpyAsync(const_cast<void *>(e.w), host->W, wb, cudaMemcpyHostToDevice,
                             p->copy_in) == cudaSuccess &&
+            cudaEventRecord(s.in_fwd, p->copy_in) == cudaSuccess &&
+            cudaStreamWaitEvent(p->copy_in, s.bwd_done, 0) == cudaSuccess &&
             cudaMemcpyAsync(dev->dY, host->dY, gb, cudaMemcpyHostToDevice, p->copy_in) ==
                 cudaSuccess &&
-            cudaEventRecord(s.in_done, p->copy_in) == cudaSuccess &&
-            cudaStreamWaitEvent(p->compute, s.in_done, 0) == cudaSuccess &&
-            cudaStreamWaitEvent(p->compute, s.out_done, 0) == cudaSuccess;
+            cudaEventRecord(s.in_bwd, p->copy_in) == cudaSuccess &&
+            // forward: its inputs are in, and the previous Y has left the device
+            cudaStreamWaitEvent(p->compute, s.in_fwd, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(p->compute, s.out_fwd, 0) == cudaSuccess;
   if (!ok) return FP8_ERR_CUDA;
   fp8_stream_t cst = reinterpret_cast<fp8_stream_t>(p->compute);
   st = fp8_weight_cache_get(cache, h, w_version, 1, cst, nullptr);
   if (st == FP8_OK)
     st = fp8_linear_fwd(dev->X, N, K, cache, h, recipe, dev->Y, dev->ctx, dev->ws, dev->ws_bytes,
                         cst);
-  if (st == FP8_OK)
-    st = fp8_linear_bwd(dev->dY, N, O, dev->ctx, cache, h, recipe, dev->dX, dev->dW, dev->ws,
-                        dev->ws_bytes, cst);
   if (st != FP8_OK) return st;
-  ok = cudaEventRecord(s.compute_done, p->compute) == cudaSuccess &&
-       cudaStreamWaitEvent(p->copy_out, s.compute_done, 0) == cudaSuccess &&
+  // backward: dY is in, and the previous dX and dW have left the device
+  ok = cudaEventRecord(s.fwd_done, p->compute) == cudaSuccess &&
+       cudaStreamWaitEvent(p->compute, s.in_bwd, 0) == cudaSuccess &&
+       cudaStreamWaitEvent(p->compute, s.out_bwd, 0) == cudaSuccess;
+  if (!ok) return FP8_ERR_CUDA;
+  st = fp8_linear_bwd(dev->dY, N, O, dev->ctx, cache, h, recipe, dev->dX, dev->dW, dev->ws,
+                      dev->ws_bytes, cst);
+  if (st != FP8_OK) return st;
+  // copy-out: Y as soon as the forward is done, dX and dW after the backward
+  ok = cudaEventRecord(s.bwd_done, p->compute) == cudaSuccess &&
+       cudaStreamWaitEvent(p->copy_out, s.fwd_done, 0) == cudaSuccess &&
        cudaMemcpyAsync(host->Y, dev->Y, gb, cudaMemcpyDeviceToHost, p->copy_out) == cudaSuccess &&
+       cudaEventRecord(s.out_fwd, p->copy_out) == cudaSuccess &&
+       cudaStreamWaitEvent(p->copy_out, s.bwd_done, 0) == cudaSuccess &&
        (!host->dX || !dev->dX ||
         cudaMemcpyAsync(host->dX, dev->dX, xb, cudaMemcpyDeviceToHost, p->copy_out) ==
             cudaSuccess) &&
        cudaMemcpyAsync(host->dW, dev->dW, wb, cudaMemcpyDeviceToHost, p->copy_out) ==
            cudaSuccess &&
-       cudaEventRecord(s.out_done, p->copy_out) == cudaSuccess;
+       cudaEventRecord(s.out_bwd, p->copy_out) == cudaSuccess;
   return ok ? FP8_OK : FP8_ERR_CUDA;
 }
 

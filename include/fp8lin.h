@@ -342,13 +342,17 @@ fp8_status fp8_grad_accumulate(float *acc, const void *dW, int64_t n, fp8_stream
  * A pipeline owns three CUDA streams on the device current at creation
  * (copy-in, compute, copy-out) and `slots` sets of events.  Each slot stands
  * for one set of device buffers (one linear).  fp8_linear_step_host(slot):
- *   copy-in:  X, W, dY host -> device (W into the buffer registered for the
- *             weight handle), after this slot's previous compute has finished
- *             reading them;
- *   compute:  fp8_weight_cache_get(h, w_version, use_cache = 1), then
- *             fp8_linear_fwd and fp8_linear_bwd, after this slot's copy-in
- *             and after this slot's previous results have left the device;
- *   copy-out: Y, dX (if both pointers are set), dW device -> host.
+ *   copy-in:  X, W host -> device (W into the buffer registered for the
+ *             weight handle) once this slot's previous forward has read them,
+ *             then dY once this slot's previous backward has read it;
+ *   compute:  fp8_weight_cache_get(h, w_version, use_cache = 1) and
+ *             fp8_linear_fwd once X and W are in and this slot's previous Y
+ *             has left the device; fp8_linear_bwd once dY is in and this
+ *             slot's previous dX and dW have left the device;
+ *   copy-out: Y as soon as the forward has finished, then dX (if both
+ *             pointers are set) and dW after the backward.
+ * So within one call dY streams in while the forward runs and Y streams out
+ * while the backward runs.
  * Calls on different slots overlap: the copies of one linear run while
  * another's kernels execute.  The compute work of all slots is ordered on the
  * one compute stream, so `ctx` and `ws` may be shared by all slots; the

@@ -87,6 +87,58 @@ def test_host_steps_equal_device_path(fp, recipe):
     check_gemm(host["Y"], A @ B.T, np.abs(A) @ np.abs(B).T, SHAPES[0][0], "Y (host step)")
 
 
+def test_host_steps_back_to_back(fp):
+    """Three steps enqueued without a sync in between (every slot's device
+    buffers reused from step to step, the forward and backward halves of a
+    step ordered against the previous step's copies by the pipeline's
+    events): every step's host results equal the device path's bit for bit."""
+    from fp8_mixed_precision_gb300 import synthetic as syn
+    dev = torch.device("cuda")
+    recipe, N, steps = "tensorwise", 4096, 3
+    pipe = fp.HostPipeline(len(SHAPES))
+    cache_h, cache_d = fp.WeightCache(), fp.WeightCache()
+    ws = max((fp.linear_workspace(recipe, N, K, O, dev) for K, O in SHAPES), key=lambda t: t.numel())
+    ctx = fp.LinearContext(fp._empty_bytes(max(fp._ctx_bytes(recipe, N, K) for K, _ in SHAPES), dev),
+                           N, 512)
+    slots = []
+    for K, O in SHAPES:
+        wd_h = torch.empty((O, K), dtype=torch.bfloat16, device=dev)
+        wd_d = torch.empty((O, K), dtype=torch.bfloat16, device=dev)
+        slots.append(dict(K=K, O=O, h_h=cache_h.register(wd_h, recipe),
+                          h_d=cache_d.register(wd_d, recipe), wd_d=wd_d,
+                          dev={k: torch.empty(sh, dtype=torch.bfloat16, device=dev) for k, sh in
+                               (("X", (N, K)), ("dY", (N, O)), ("Y", (N, O)), ("dX", (N, K)),
+                                ("dW", (O, K)))}))
+    hosts = []
+    for step in range(steps):
+        cache_h.begin_cycle()
+        row = []
+        for i, s in enumerate(slots):
+            K, O = s["K"], s["O"]
+            seed = 1000 + 100 * step + 10 * i
+            host = {"X": syn.bf16_normal((N, K), 1.0, seed + 1).pin_memory(),
+                    "W": syn.bf16_normal((O, K), 0.02, seed + 2).pin_memory(),
+                    "dY": syn.bf16_normal((N, O), 1e-3, seed + 3).pin_memory(),
+                    "Y": torch.empty((N, O), dtype=torch.bfloat16).pin_memory(),
+                    "dX": torch.empty((N, K), dtype=torch.bfloat16).pin_memory(),
+                    "dW": torch.empty((O, K), dtype=torch.bfloat16).pin_memory()}
+            pipe.step(i, host, s["dev"], ctx, ws, cache_h, s["h_h"], recipe, version=step + 1)
+            row.append(host)
+        hosts.append(row)
+    pipe.sync()
+    assert fp.fp8_get_device_status() == 0
+    for step, row in enumerate(hosts):
+        cache_d.begin_cycle()
+        for i, (s, host) in enumerate(zip(slots, row)):
+            s["wd_d"].copy_(host["W"].to(dev))
+            cache_d.get(s["h_d"], step + 1, True)
+            y, c = fp.fp8_linear_fwd(host["X"].to(dev), cache_d, s["h_d"], recipe)
+            dx, dw = fp.fp8_linear_bwd(host["dY"].to(dev), c, cache_d, s["h_d"], recipe)
+            torch.cuda.synchronize()
+            for nm, got, exp in (("Y", host["Y"], y), ("dX", host["dX"], dx), ("dW", host["dW"], dw)):
+                assert torch.equal(_bits(got), _bits(exp.cpu())), f"{nm} slot {i} step {step}"
+
+
 def test_host_step_rejects_before_enqueue(fp):
     dev = torch.device("cuda")
     pipe = fp.HostPipeline(1)
