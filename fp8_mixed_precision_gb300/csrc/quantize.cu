@@ -253,6 +253,11 @@ __global__ void __launch_bounds__(kQThreads, 2)
     }
   };
 
+  // the first tiles do not depend on the scale: request them now
+  int64_t id = blockIdx.x;
+  prefetch(id, 0);
+  if (PRE != 2) prefetch(id + gridDim.x, 1);
+
   float ts = 1.0f, tsi = 1.0f;
   if (MODE == Q_TENSOR) {
     float a = 0.0f;
@@ -286,9 +291,6 @@ __global__ void __launch_bounds__(kQThreads, 2)
   const bool want_row = p.out_row != nullptr;
   const bool want_col = p.out_col != nullptr;
   uint32_t cur_max = 0;  // delayed: running |max| of this CTA's tiles (bf16 pair)
-  int64_t id = blockIdx.x;
-  prefetch(id, 0);
-  if (PRE != 2) prefetch(id + gridDim.x, 1);
   for (int k = 0; id < ntiles; ++k, id += gridDim.x) {
     const int b = PRE == 2 ? 0 : (k & 1);
     uint16_t *in = S.in[b];
