@@ -1049,7 +1049,8 @@ def run_plain_and_assay(fp, dev, stream):
         out["plain_vs_fused"][f"{K}->{O}"] = {"fused_ms": ms_f, "plain_ms": ms_p,
                                               "fused_speedup": ms_p / ms_f,
                                               "outputs_bitwise_equal": bool(same)}
-        # GEMM-only assay: the three GEMMs of the linear, FP8 vs bf16 cuBLAS
+        # GEMM-only assay: the three GEMMs of the linear, ours (FP8) against bf16
+        # cuBLAS and against cuBLAS FP8 on the same operands (library context)
         xq = fp.fp8_quantize(x, RECIPE, "act")
         wq = fp.fp8_quantize(w, RECIPE, "weight")
         gq = fp.fp8_quantize(dy, RECIPE, "grad")
@@ -1064,9 +1065,25 @@ def run_plain_and_assay(fp, dev, stream):
             torch.matmul(dy, w)
             torch.matmul(dy.t(), x)
 
+        def gc8():  # the same FP8 operands and scales through cuBLAS (torch._scaled_mm)
+            f8 = lambda t, f: t.view(torch.float8_e4m3fn if f == "e4m3" else torch.float8_e5m2)
+            sx, sw, sg = (xq["row_scale_inv"].reshape(()), wq["row_scale_inv"].reshape(()),
+                          gq["row_scale_inv"].reshape(()))
+            torch._scaled_mm(f8(xq["row"], "e4m3"), f8(wq["row"], "e4m3").t(), scale_a=sx, scale_b=sw,
+                             out_dtype=torch.bfloat16)
+            torch._scaled_mm(f8(gq["row"], "e5m2"), f8(wq["col"], "e4m3").t(), scale_a=sg, scale_b=sw,
+                             out_dtype=torch.bfloat16)
+            torch._scaled_mm(f8(gq["col"], "e5m2"), f8(xq["col"], "e4m3").t(), scale_a=sg, scale_b=sx,
+                             out_dtype=torch.bfloat16)
+
         ms8, ms16 = timed(g8), timed(g16)
-        out["gemm_assay"][f"{K}->{O}"] = {"fp8_ms": ms8, "bf16_cublas_ms": ms16,
-                                          "bf16_over_fp8": ms16 / ms8}
+        ent = {"fp8_ms": ms8, "bf16_cublas_ms": ms16, "bf16_over_fp8": ms16 / ms8}
+        try:
+            msc = timed(gc8)
+            ent.update(cublas_fp8_ms=msc, cublas_fp8_over_ours=msc / ms8)
+        except (RuntimeError, AttributeError, TypeError) as e:  # library FP8 path unavailable
+            ent.update(cublas_fp8_ms=None, cublas_fp8_note=str(e).splitlines()[0][:120])
+        out["gemm_assay"][f"{K}->{O}"] = ent
         # memory: saved for backward and peak of one fwd+bwd
         ctx_b = fp._ctx_bytes(RECIPE, N, K)
         res.clear()
@@ -1099,6 +1116,9 @@ def run_plain_and_assay(fp, dev, stream):
         sum(a[s]["bf16_cublas_ms"] for s in mlp) / sum(a[s]["fp8_ms"] for s in mlp))
     out["gemm_assay"]["summed_bf16_over_fp8_square"] = (
         sum(a[s]["bf16_cublas_ms"] for s in sq) / sum(a[s]["fp8_ms"] for s in sq))
+    if all(a[s].get("cublas_fp8_ms") for s in mlp + sq):
+        out["gemm_assay"]["summed_cublas_fp8_over_ours"] = (
+            sum(a[s]["cublas_fp8_ms"] for s in mlp + sq) / sum(a[s]["fp8_ms"] for s in mlp + sq))
     return out
 
 
