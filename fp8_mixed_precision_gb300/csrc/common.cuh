@@ -93,7 +93,8 @@ __device__ __forceinline__ bool any_nonfinite_bf16(uint4 a, uint4 b) {
 // results bf16 can hold) and the product is scaled by 2^-64 last, so tiny
 // results round once, subnormals included.  The arithmetic runs on packed
 // fp32 pairs (f32x2: one instruction, two IEEE operations); the reciprocal
-// (the hardware's approximate one) and the exponential are per element.
+// and the base-2 exponential, the hardware's approximate instructions, are
+// per element.
 // Every finite bf16 input lands within 1 bf16 ulp of the exact value (tested
 // over all of them).
 namespace gelu2 {
@@ -116,26 +117,31 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
   return d;
 }
 __device__ __forceinline__ uint64_t dup(float a) { return pk(a, a); }
-// tq = t Q(t) ~ erfcx(z) and e64 = 2^64 exp(-z^2) for z = |h| / sqrt 2, both elements
+// For z = |h| / sqrt 2, both elements: tq = t Q(t) / 2 ~ erfcx(z) / 2 and e64 = 2^64 exp(-z^2).
+// The 1/sqrt 2 is folded into the constants (d = 1 + |h| / (2 sqrt 2), exponent 64 - h^2 log2(e) / 2)
+// and the 1/2 into Q's coefficients, both exact or within a rounding of the unfolded forms.
 __device__ __forceinline__ void parts(float h0, float h1, uint64_t &tq, uint64_t &e64) {
-  const uint64_t z = mul2(pk(fabsf(h0), fabsf(h1)), dup(0.70710678118654752f));
+  const uint64_t a = pk(fabsf(h0), fabsf(h1));
   float d0, d1;
-  upk(fma2(z, dup(0.5f), dup(1.0f)), d0, d1);
+  upk(fma2(a, dup(0.35355339059327376f), dup(1.0f)), d0, d1);
   float t0, t1;  // the hardware's approximate reciprocal (within 1 ulp of 1/d)
   asm("rcp.approx.f32 %0, %1;" : "=f"(t0) : "f"(d0));
   asm("rcp.approx.f32 %0, %1;" : "=f"(t1) : "f"(d1));
   const uint64_t t = pk(t0, t1);
-  uint64_t q = fma2(dup(0.050986580550670624f), t, dup(-0.11058920621871948f));
-  q = fma2(q, t, dup(-0.040473274886608124f));
-  q = fma2(q, t, dup(0.12493661046028137f));
-  q = fma2(q, t, dup(0.1622200757265091f));
-  q = fma2(q, t, dup(0.24883142113685608f));
-  q = fma2(q, t, dup(0.28199517726898193f));
-  q = fma2(q, t, dup(0.2820955216884613f));
+  uint64_t q = fma2(dup(0.025493290275335312f), t, dup(-0.05529460310935974f));
+  q = fma2(q, t, dup(-0.020236637443304062f));
+  q = fma2(q, t, dup(0.062468305230140686f));
+  q = fma2(q, t, dup(0.08111003786325455f));
+  q = fma2(q, t, dup(0.12441571056842804f));
+  q = fma2(q, t, dup(0.14099758863449097f));
+  q = fma2(q, t, dup(0.14104776084423065f));
   tq = mul2(t, q);
   float a0, a1;
-  upk(fma2(mul2(z, z), dup(-1.4426950408889634f), dup(64.0f)), a0, a1);
-  e64 = pk(exp2f(a0), exp2f(a1));
+  upk(fma2(mul2(a, a), dup(-0.72134752044448170f), dup(64.0f)), a0, a1);
+  float x0, x1;  // the hardware's approximate base-2 exponential (relative error ~2^-22)
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(x0) : "f"(a0));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(x1) : "f"(a1));
+  e64 = pk(x0, x1);
 }
 }  // namespace gelu2
 
@@ -145,7 +151,7 @@ __device__ __forceinline__ void gelu_f2(float h0, float h1, float &g0, float &g1
   uint64_t tq, e64;
   parts(h0, h1, tq, e64);
   // h erfc(z) / 2
-  const uint64_t hq = mul2(mul2(mul2(mul2(pk(h0, h1), dup(0.5f)), tq), e64), dup(5.42101086242752217e-20f));
+  const uint64_t hq = mul2(mul2(mul2(pk(h0, h1), tq), e64), dup(5.42101086242752217e-20f));
   float q0, q1;
   upk(hq, q0, q1);
   g0 = h0 >= 0.0f ? __fsub_rn(h0, q0) : q0;
@@ -157,7 +163,7 @@ __device__ __forceinline__ void gelu_grad_f2(float h0, float h1, float &g0, floa
   uint64_t tq, e64;
   parts(h0, h1, tq, e64);
   // h >= 0: 1 - erfc(z)/2 + h phi(h);  h < 0: erfc(z)/2 + h phi(h)
-  const uint64_t s = pk(h0 >= 0.0f ? -0.5f : 0.5f, h1 >= 0.0f ? -0.5f : 0.5f);
+  const uint64_t s = pk(h0 >= 0.0f ? -1.0f : 1.0f, h1 >= 0.0f ? -1.0f : 1.0f);
   const uint64_t v = mul2(mul2(fma2(s, tq, mul2(pk(h0, h1), dup(0.39894228040143268f))), e64),
                           dup(5.42101086242752217e-20f));
   float v0, v1;
