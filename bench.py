@@ -388,7 +388,8 @@ def run_ours(args):
     # The same work with the tensorwise amax passes of X and dY (pure HBM
     # reads, almost no shared memory) on a second stream, where their CTAs run
     # beside the GEMM and cast CTAs of earlier linears; each cast waits for its
-    # tensor's partial maxima.  Results are bit for bit those of step_serial.
+    # tensor's partial maxima.  Results are bit for bit those of step_serial
+    # (checked below on the captured graphs).
     stream = torch.cuda.current_stream()
     aux = torch.cuda.Stream(dev)
     px = [fp.amax_partials_buffer(N, L["K"], dev) for L in layers]
@@ -398,9 +399,10 @@ def run_ours(args):
     ev_dy = [torch.cuda.Event() for _ in layers]
 
     def step_overlap():
+        cur = torch.cuda.current_stream()   # the capture stream while a graph is recorded
         cache.begin_cycle()
         version[0] += 1
-        ev_go.record(stream)          # earlier casts are done with the partial buffers
+        ev_go.record(cur)             # earlier casts are done with the partial buffers
         aux.wait_event(ev_go)
         with torch.cuda.stream(aux):
             for i, L in enumerate(layers):
@@ -411,9 +413,9 @@ def run_ours(args):
         for i, L in enumerate(layers):
             cache.get(L["h"], version[0], True)
             c = fp.LinearContext(ctx.ctx, N, L["K"])
-            stream.wait_event(ev_x[i])
+            cur.wait_event(ev_x[i])
             fp.fp8_linear_fwd_after_amax(L["x"], px[i], cache, L["h"], RECIPE, ws, L["y"], c)
-            stream.wait_event(ev_dy[i])
+            cur.wait_event(ev_dy[i])
             fp.fp8_linear_bwd_after_amax(L["dy"], pdy[i], c, cache, L["h"], RECIPE, ws, L["dx"],
                                          L["dw"])
 
@@ -441,19 +443,44 @@ def run_ours(args):
 
     # One step captured in a CUDA graph: every replay runs the same kernels
     # with the same arguments (the weights are re-quantized each replay, as in
-    # the eager step), without the host's per-launch work between them.
-    graph = torch.cuda.CUDAGraph()
-    side = torch.cuda.Stream(dev)
-    side.wait_stream(stream)
-    with torch.cuda.stream(side):
-        step()                          # warm the capture stream
-    stream.wait_stream(side)
-    torch.cuda.synchronize()
-    with torch.cuda.graph(graph):
-        step()
-    torch.cuda.synchronize()
+    # the eager step), without the host's per-launch work between them.  Each
+    # schedule gets its own graph.
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            fn()                        # warm the capture stream
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        return g
+    other_fn = step_serial if args.schedule == "overlap" else step_overlap
+    graph = capture(step)
+    other_graph = capture(other_fn) if args.launch == "graph" else None
     eager_step = step
     timed_step = graph.replay if args.launch == "graph" else eager_step
+
+    # Both schedules, as they are timed, against one eager serial step: every
+    # output bit for bit.
+    step_serial()
+    torch.cuda.synchronize()
+    ref = [t.clone() for L in layers for t in (L["y"], L["dx"], L["dw"])]
+    schedules_equal = True
+    for run in (timed_step, other_graph.replay if other_graph is not None else other_fn):
+        for L in layers:
+            for t in (L["y"], L["dx"], L["dw"]):
+                t.zero_()
+        run()
+        torch.cuda.synchronize()
+        got = [t for L in layers for t in (L["y"], L["dx"], L["dw"])]
+        schedules_equal = schedules_equal and all(
+            torch.equal(a.view(torch.int16), b.view(torch.int16)) for a, b in zip(ref, got))
+    del ref
+    if not schedules_equal:
+        raise RuntimeError("the two schedules' outputs differ")
     for _ in range(args.warmup):
         timed_step()
     torch.cuda.synchronize()
@@ -492,14 +519,15 @@ def run_ours(args):
     torch.cuda.synchronize()
     fp.fp8_profile_begin()
     p0.record(stream)
-    for _ in range(args.steps):
-        eager_step()
+    for _ in range(args.steps):         # one stream: no kernel shares the GPU with another
+        step_serial()
     p1.record(stream)
     torch.cuda.synchronize()
     krecs = fp.fp8_profile_end(by_shape=True)
     profiled_ms_step = p0.elapsed_time(p1) / args.steps
-    # the other schedule, for reference (same work, same results)
-    other = step_serial if args.schedule == "overlap" else step_overlap
+    # the other schedule, for reference (same work, same results), launched
+    # the same way
+    other = other_graph.replay if other_graph is not None else other_fn
     o0, o1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     o0.record(stream)
@@ -518,7 +546,7 @@ def run_ours(args):
     q1.record(stream)
     torch.cuda.synchronize()
     other_launch_ms = reduce_max(q0.elapsed_time(q1), world, dev) / args.steps
-    del graph
+    del graph, other_graph
     ms_local = t0.elapsed_time(t1)
     ms_total = reduce_max(ms_local, world, dev)
     ms_step = ms_total / args.steps
@@ -561,7 +589,8 @@ def run_ours(args):
                      "note": "sum over the step's launches of max(flops / FP8 burst peak, "
                              "algorithmic bytes / HBM peak), against the measured step time"},
             "timing": ("CUDA events around each launch on its stream, over a second region of "
-                       "the same K steps (value comes from an event-free region)")}
+                       "the same K steps, eager, every kernel on one stream (value comes "
+                       "from an event-free region)")}
 
     # ---- end to end through the C ABI with host buffers
     e2e = run_e2e(fp, layers, cache, ws, ctx, N, dev, world, args, stream)
@@ -617,9 +646,11 @@ def run_ours(args):
                                     "GEMMs and casts" if args.schedule == "overlap"
                                     else "one stream"),
                        "launch": ("one step captured as a CUDA graph, replayed"
-                                  if args.launch == "graph" else "eager launches")},
+                                  if args.launch == "graph" else "eager launches"),
+                       "programmatic_dependent_launch": os.environ.get("FP8LIN_PDL", "1")[:1] != "0"},
             "other_schedule_ms_per_step": {("serial" if args.schedule == "overlap"
                                             else "overlap"): other_ms_step},
+            "schedules_bitwise_equal": schedules_equal,
             "profiled_ms_per_step": profiled_ms_step,
             "other_launch_ms_per_step": {("eager" if args.launch == "graph" else "graph"):
                                          other_launch_ms},
@@ -1218,8 +1249,9 @@ def main(argv=None):
     ap.add_argument("--launch", choices=["graph", "eager"], default="graph",
                     help="graph (default): time replays of one step captured as a CUDA graph; "
                          "eager: one library call per linear per step")
-    ap.add_argument("--schedule", choices=["serial", "overlap"], default="serial",
-                    help="overlap: tensorwise amax passes on a second stream")
+    ap.add_argument("--schedule", choices=["serial", "overlap"], default="overlap",
+                    help="overlap (default): tensorwise amax passes on a second stream; "
+                         "serial: every kernel on one stream")
     ap.add_argument("--no-mlp", action="store_true",
                     help="skip the MLP-level workloads reported beside the main line")
     ap.add_argument("--oracle-timing", default=None, help=argparse.SUPPRESS)

@@ -31,6 +31,23 @@ __device__ __forceinline__ void scale_from_amax(float amax, float fmax, float &s
   s_inv = __fdiv_rn(1.0f, s);
 }
 
+// Programmatic dependent launch.  Every kernel of this library calls one of
+// these before its first global-memory access (after its barrier setup,
+// descriptor prefetch and TMEM allocation): the thread waits until the kernel
+// before it on the stream has completed with its memory visible (at once when
+// the launch did not allow overlap).  Results are those of serial launches.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// ... and then lets the next kernel's CTAs start their own setup on whatever
+// SM resources are free.  The GEMM does not release early: the small kernels
+// that follow it (amax pass, split-K reduce, gradient accumulation) fit beside
+// a running GEMM CTA, and with an early release the step ran slower (fp8
+// linear step at N = 131072 on four shapes: 3.84 ms with the GEMM releasing
+// at exit, 3.93 ms with it releasing at once).
+__device__ __forceinline__ void pdl_wait_then_release() {
+  pdl_wait();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // |x| max that ignores NaN (fmaxf returns the non-NaN operand).
 __device__ __forceinline__ float amax_acc(float acc, float v) { return fmaxf(acc, fabsf(v)); }
 

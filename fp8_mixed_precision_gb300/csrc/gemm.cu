@@ -376,6 +376,7 @@ __global__ void __launch_bounds__(Cfg<SCALING, SPLIT, BN, MH, PR>::kThreads, 1)
   __syncthreads();
   if (PR) ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
   ptx::tc_fence_after();
+  pdl_wait();  // dependents launch as this grid exits
   const uint32_t tmem = ctl->tmem_base;
   volatile int *abort = &ctl->abort;
 
@@ -954,6 +955,7 @@ __global__ void wait_timeout_probe_kernel(uint64_t limit_ns) {
 // Fixed-order sum of the split-K partials, rounded once to bf16.
 __global__ void splitk_reduce_kernel(const float *__restrict__ ws, int splits, int64_t mn,
                                      __nv_bfloat16 *__restrict__ C) {
+  pdl_wait_then_release();
   const int64_t n4 = mn / 4;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -1113,7 +1115,7 @@ cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const C
   constexpr int kCl = PR ? 2 : 1;  // CTAs per cluster
   auto kernel = fp8_gemm_kernel<SCALING, SPLIT, BN, MH, PR>;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kCl;
   attr[0].val.clusterDim.y = 1;
@@ -1122,7 +1124,7 @@ cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const C
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = PR ? 1 : 0;
+  cfg.numAttrs = PR ? 1 : 0;  // the occupancy query below sees the cluster shape only
   // per device: the shared-memory opt-in, and how many CTAs can be resident
   // at once (whole clusters for pairs), which sizes the persistent grid
   static int resident[64] = {0};
@@ -1159,6 +1161,11 @@ cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const C
   if (SCALING == FP8_SCALING_1x128_1x128) bytes += 4.0 * g.kbs * (g.M + g.N);
   LaunchScope ls(names[SCALING], st, bytes, 2.0 * g.M * g.N * g.K, g.M, g.N, g.K);
   cfg.gridDim = dim3((unsigned)grid);
+  if (pdl_enabled()) {
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    ++cfg.numAttrs;
+  }
   return cudaLaunchKernelEx(&cfg, kernel, ta, tb, tc, g);
 }
 
@@ -1269,12 +1276,14 @@ cudaError_t launch_gemm(const uint8_t *A, int a_fmt, const float *a_sinv, const 
   }
   if (e != cudaSuccess || !split) return e;
   const int64_t mn = M * N;
-  const int64_t blocks = std::min<int64_t>((mn / 4 + 255) / 256, (int64_t)num_sms() * 8);
+  static int reduce_bps[64];
+  const int64_t blocks = std::min<int64_t>(
+      (mn / 4 + 255) / 256, (int64_t)num_sms() * blocks_per_sm(splitk_reduce_kernel, 256, reduce_bps));
   LaunchScope ls("gemm_splitk_reduce", st, 4.0 * p.splits * mn + 2.0 * mn, (double)p.splits * mn, M, N,
                  p.splits);
-  splitk_reduce_kernel<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, st>>>(
-      static_cast<const float *>(ws), p.splits, mn, static_cast<__nv_bfloat16 *>(Cout));
-  return cudaGetLastError();
+  return launch_kernel(splitk_reduce_kernel, dim3((unsigned)std::max<int64_t>(blocks, 1)), dim3(256),
+                       0, st, static_cast<const float *>(ws), p.splits, mn,
+                       static_cast<__nv_bfloat16 *>(Cout));
 }
 
 cudaError_t launch_wait_timeout_probe(uint64_t limit_ns, cudaStream_t st) {

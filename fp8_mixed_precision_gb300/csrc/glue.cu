@@ -40,10 +40,12 @@ __device__ __forceinline__ uint4 gelu_bwd8(uint4 d, uint4 h) {
 
 // Grid-stride over 8-element vectors on a grid of exactly the resident
 // blocks, at full occupancy (32 registers: 8 blocks of 256 threads per SM).
-// Measured on 131072 x 2048: forward 0.255 ms, backward 0.293 ms; two
-// vectors per iteration at 40-52 registers ran 0.267 / 0.314-0.339 ms.
+// Measured on 131072 x 2048 with an earlier form of the GELU arithmetic:
+// forward 0.255 ms, backward 0.293 ms; two vectors per iteration at 40-52
+// registers ran 0.267 / 0.314-0.339 ms.
 __global__ void __launch_bounds__(kThreads, 8) gelu_fwd_kernel(const uint4 *__restrict__ H,
                                                                uint4 *__restrict__ A, int64_t n8) {
+  pdl_wait_then_release();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride)
     A[i] = gelu8(H[i]);
@@ -52,6 +54,7 @@ __global__ void __launch_bounds__(kThreads, 8) gelu_fwd_kernel(const uint4 *__re
 __global__ void __launch_bounds__(kThreads, 8) gelu_bwd_kernel(const uint4 *__restrict__ dA,
                                                                const uint4 *__restrict__ H,
                                                                uint4 *__restrict__ dH, int64_t n8) {
+  pdl_wait_then_release();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride)
     dH[i] = gelu_bwd8(dA[i], H[i]);
@@ -59,6 +62,7 @@ __global__ void __launch_bounds__(kThreads, 8) gelu_bwd_kernel(const uint4 *__re
 
 __global__ void grad_accumulate_kernel(float4 *__restrict__ acc, const uint2 *__restrict__ dW,
                                        int64_t n4) {
+  pdl_wait_then_release();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
        i += (int64_t)gridDim.x * blockDim.x) {
     float4 a = acc[i];
@@ -71,32 +75,16 @@ __global__ void grad_accumulate_kernel(float4 *__restrict__ acc, const uint2 *__
   }
 }
 
-unsigned grid_for(int64_t items) {
-  const int64_t want = (items + kThreads - 1) / kThreads;
-  return (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms() * 8));
-}
-
-// Grid of the GELU kernels: every block resident at once (blocks per SM from
+// Grid of the glue kernels: every block resident at once (blocks per SM from
 // the occupancy calculator, per kernel and device), so that no block starts
 // after the others have finished their grid-stride share.
 template <typename Kernel>
 unsigned grid_resident(Kernel kernel, int64_t items, int *per_dev) {
-  int dev = 0;
-  cudaGetDevice(&dev);
-  int bps = 8;
-  if (dev >= 0 && dev < 64) {
-    if (per_dev[dev] == 0) {
-      int n = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, 0) != cudaSuccess || n < 1)
-        n = 1;
-      per_dev[dev] = n;
-    }
-    bps = per_dev[dev];
-  }
+  const int bps = blocks_per_sm(kernel, kThreads, per_dev);
   const int64_t want = (items + kThreads - 1) / kThreads;
   return (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms() * bps));
 }
-int g_gelu_fwd_bps[64], g_gelu_bwd_bps[64];
+int g_gelu_fwd_bps[64], g_gelu_bwd_bps[64], g_acc_bps[64];
 
 }  // namespace
 
@@ -104,25 +92,25 @@ cudaError_t launch_gelu_fwd(const void *H, void *A, int64_t n, cudaStream_t st) 
   const int64_t n8 = n / 8;
   LaunchScope ls("gelu_fwd", st, 4.0 * n, 0.0, n);
   const unsigned grid = grid_resident(gelu_fwd_kernel, n8, g_gelu_fwd_bps);
-  gelu_fwd_kernel<<<grid, kThreads, 0, st>>>(static_cast<const uint4 *>(H), static_cast<uint4 *>(A), n8);
-  return cudaGetLastError();
+  return launch_kernel(gelu_fwd_kernel, dim3(grid), dim3(kThreads), 0, st,
+                       static_cast<const uint4 *>(H), static_cast<uint4 *>(A), n8);
 }
 
 cudaError_t launch_gelu_bwd(const void *dA, const void *H, void *dH, int64_t n, cudaStream_t st) {
   const int64_t n8 = n / 8;
   LaunchScope ls("gelu_bwd", st, 6.0 * n, 0.0, n);
   const unsigned grid = grid_resident(gelu_bwd_kernel, n8, g_gelu_bwd_bps);
-  gelu_bwd_kernel<<<grid, kThreads, 0, st>>>(static_cast<const uint4 *>(dA), static_cast<const uint4 *>(H),
-                                             static_cast<uint4 *>(dH), n8);
-  return cudaGetLastError();
+  return launch_kernel(gelu_bwd_kernel, dim3(grid), dim3(kThreads), 0, st,
+                       static_cast<const uint4 *>(dA), static_cast<const uint4 *>(H),
+                       static_cast<uint4 *>(dH), n8);
 }
 
 cudaError_t launch_grad_accumulate(float *acc, const void *dW, int64_t n, cudaStream_t st) {
   const int64_t n4 = n / 4;
   LaunchScope ls("grad_accumulate", st, 10.0 * n, (double)n, n);
-  grad_accumulate_kernel<<<grid_for(n4), kThreads, 0, st>>>(
-      reinterpret_cast<float4 *>(acc), static_cast<const uint2 *>(dW), n4);
-  return cudaGetLastError();
+  const unsigned grid = grid_resident(grad_accumulate_kernel, n4, g_acc_bps);
+  return launch_kernel(grad_accumulate_kernel, dim3(grid), dim3(kThreads), 0, st,
+                       reinterpret_cast<float4 *>(acc), static_cast<const uint2 *>(dW), n4);
 }
 
 }  // namespace fp8lin

@@ -35,6 +35,54 @@ class LaunchScope {
 constexpr int kMaxPartials = 1024;
 
 int num_sms();
+
+// Kernel launches allow programmatic dependent launch (the kernel may be
+// scheduled while the previous kernel on the stream drains; each kernel waits
+// for it in pdl_wait_then_release before touching global memory) unless the
+// environment sets FP8LIN_PDL=0 when the library first launches.
+bool pdl_enabled();
+
+// Blocks of `kernel` (threads per block, no dynamic shared memory) that fit on
+// one SM of the current device, cached per device in per_dev[64].  Grids of
+// grid-stride kernels are sized to this many blocks per SM: under overlapped
+// launch the blocks are placed on SMs in the order the previous kernel frees
+// them, and a smaller grid would crowd onto the first SMs freed.
+template <typename Kernel>
+int blocks_per_sm(Kernel kernel, int threads, int *per_dev) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 1;
+  if (per_dev[dev] == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1)
+      n = 1;
+    per_dev[dev] = n;
+  }
+  return per_dev[dev];
+}
+
+// overlap = false: a plain launch (the kernel starts once the previous one on
+// the stream has completed).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel_as(bool overlap, void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                             size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap && pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, Args... args) {
+  return launch_kernel_as(true, kernel, grid, block, smem, st, args...);
+}
 int tensorwise_partials_count(int64_t rows, int64_t cols);
 
 // mode: 0 tensorwise, 1 1x128 blocks, 2 128x128 tiles; fmt: fp8_format.

@@ -39,6 +39,7 @@
 // absent elements are zero-filled by the TMA load (zeros never raise an amax)
 // and never stored.  Every wait on a tile is bounded: on expiry the kernel
 // records FP8_ERR_TIMEOUT in its status word and carries on (no trap).
+#include <cstdlib>
 #include <type_traits>
 
 #include "common.cuh"
@@ -66,6 +67,7 @@ __device__ __forceinline__ int swz(int r) { return ((r >> 4) & 7) << 2; }
 __global__ void __launch_bounds__(kAmaxThreads) amax_partials_kernel(const uint4 *__restrict__ x,
                                                                      int64_t n16,
                                                                      float *__restrict__ partials) {
+  pdl_wait_then_release();
   uint32_t m = 0;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -236,6 +238,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
     if (PRE == 2) ptx::tma_prefetch_desc(&tmx2);
   }
   __syncthreads();
+  pdl_wait_then_release();
   // Thread 0 loads tile `id` into buffer b with one TMA tensor load (two for
   // the fused GELU backward: dA into buffer 0, H into buffer 1, both on
   // barrier 0); parts of the box outside the tensor arrive as zeros.
@@ -547,6 +550,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
 __global__ void delayed_history_update_kernel(const float *__restrict__ partials, int n,
                                               float *__restrict__ hist, int hist_len,
                                               int64_t step) {
+  pdl_wait_then_release();
   __shared__ float red[8];
   float a = 0.0f;
   for (int k = threadIdx.x; k < n; k += blockDim.x) a = fmaxf(a, partials[k]);
@@ -564,6 +568,14 @@ __global__ void delayed_history_update_kernel(const float *__restrict__ partials
 // ---------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char *e = getenv("FP8LIN_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
 int num_sms() {
   static int cached[64] = {0};
   int dev = 0;
@@ -577,10 +589,14 @@ int num_sms() {
   return cached[dev];
 }
 
+static int g_amax_bps[64];
+
 int tensorwise_partials_count(int64_t rows, int64_t cols) {
   const int64_t n16 = rows * cols / 8;
   const int64_t want = (n16 + (int64_t)kAmaxThreads * 4 - 1) / ((int64_t)kAmaxThreads * 4);
-  const int64_t cap = std::min<int64_t>(2 * (int64_t)num_sms(), kMaxPartials);
+  // every SM filled: as many blocks as fit on one, times the SMs
+  const int64_t cap = std::min<int64_t>(
+      (int64_t)blocks_per_sm(amax_partials_kernel, kAmaxThreads, g_amax_bps) * num_sms(), kMaxPartials);
   return (int)std::max<int64_t>(1, std::min<int64_t>(want, cap));
 }
 
@@ -619,8 +635,8 @@ static cudaError_t launch_tile(const QParams &p, cudaStream_t st) {
     bytes += 16.0;
   if (PRE == 2) bytes += 2.0 * p.R * p.C;  // the second input (H)
   LaunchScope ls(PRE ? pre_names[PRE] : names[MODE], st, bytes, 0.0, p.R, p.C);
-  quant_tile_kernel<MODE, FMT, PRE><<<(unsigned)grid, kQThreads, kQSmemBytes, st>>>(tmx, tmx2, p);
-  return cudaGetLastError();
+  return launch_kernel(quant_tile_kernel<MODE, FMT, PRE>, dim3((unsigned)grid), dim3(kQThreads),
+                       kQSmemBytes, st, tmx, tmx2, p);
 }
 
 cudaError_t quant_read_status(unsigned *status) {
@@ -634,9 +650,10 @@ cudaError_t launch_amax_partials(const void *x, int64_t rows, int64_t cols, floa
                                  cudaStream_t st) {
   const int g = tensorwise_partials_count(rows, cols);
   LaunchScope ls("quant_amax_tensorwise", st, 2.0 * rows * cols, 0.0, rows, cols);
-  amax_partials_kernel<<<g, kAmaxThreads, 0, st>>>(static_cast<const uint4 *>(x), rows * cols / 8,
-                                                   partials);
-  return cudaGetLastError();
+  // a plain launch: overlapped with the kernel before it, the step measured
+  // 0.5% slower (3.84 against 3.82 ms, fp8 linear step at N = 131072)
+  return launch_kernel_as(false, amax_partials_kernel, dim3(g), dim3(kAmaxThreads), 0, st,
+                          static_cast<const uint4 *>(x), (int64_t)(rows * cols / 8), partials);
 }
 
 cudaError_t launch_quantize(const void *x, int64_t rows, int64_t cols, int mode, int fmt,
@@ -701,8 +718,8 @@ cudaError_t launch_quantize_delayed(const void *x, int64_t rows, int64_t cols, i
                                          : launch_tile<Q_TENSOR, FP8_FORMAT_E5M2>(p, st);
   if (e != cudaSuccess) return e;
   LaunchScope ls("quant_delayed_history", st, 4.0 * grid + 4.0, 0.0);
-  delayed_history_update_kernel<<<1, 256, 0, st>>>(partials, grid, hist, hist_len, step);
-  return cudaGetLastError();
+  return launch_kernel(delayed_history_update_kernel, dim3(1), dim3(256), 0, st,
+                       (const float *)partials, (int)grid, hist, hist_len, (int64_t)step);
 }
 
 cudaError_t launch_gelu_quantize(const void *H, const void *H2, int64_t rows, int64_t cols,

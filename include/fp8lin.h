@@ -33,6 +33,11 @@
  *     fp8_get_device_status and fp8_host_pipeline_sync (fp8_linear_step_host
  *     enqueues on its pipeline's own streams).  Arguments are validated before anything is
  *     launched: on a non-OK status nothing was enqueued.
+ *   - Kernels are launched with programmatic dependent launch: a kernel may
+ *     be scheduled while the kernel before it on the same stream drains, and
+ *     waits for that kernel's completion before it touches memory, so every
+ *     result is that of serial stream order.  FP8LIN_PDL=0 in the
+ *     environment (read on the first launch) gives plain launches.
  *   - Calls are not thread-safe with respect to one fp8_weight_cache object.
  *     Other calls may come from several host threads: the per-device launch
  *     settings the library fills in on first use (shared-memory opt-in,
