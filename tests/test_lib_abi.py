@@ -185,3 +185,60 @@ def test_gemm_kernels_compile_without_spills(L):
         assert m, name
         assert m.group(1) == "0" and m.group(2) == "0", f"{name}: {m.group(0)}"
     assert seen >= 4, seen
+
+
+def _kernels():
+    """(file, kernel name, body) of every __global__ function in csrc/, with
+    comments removed."""
+    d = os.path.join(ROOT, "fp8_mixed_precision_gb300", "csrc")
+    out = []
+    for fn in sorted(os.listdir(d)):
+        if not fn.endswith((".cu", ".cuh")):
+            continue
+        src = open(os.path.join(d, fn)).read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        for m in re.finditer(r"__global__\s+void\s+(?:__launch_bounds__\s*\([^()]*\)\s*)?(\w+)\s*\(",
+                             src):
+            name, paren = m.group(1), m.end() - 1
+            depth, i = 0, paren            # skip the parameter list
+            while True:
+                depth += {"(": 1, ")": -1}.get(src[i], 0)
+                i += 1
+                if depth == 0:
+                    break
+            start = src.index("{", i)
+            depth, j = 0, start
+            while True:
+                depth += {"{": 1, "}": -1}.get(src[j], 0)
+                j += 1
+                if depth == 0:
+                    break
+            out.append((fn, name, src[start:j]))
+    return out
+
+
+def test_every_kernel_waits_for_its_predecessor():
+    """Kernels are launched with programmatic dependent launch, so each one
+    must wait (griddepcontrol.wait, through pdl_wait or
+    pdl_wait_then_release) for the kernel before it on the stream; the bounded
+    wait probe is the one kernel launched plainly."""
+    ks = _kernels()
+    assert len(ks) >= 9, [k[1] for k in ks]
+    for fn, name, body in ks:
+        if name == "wait_timeout_probe_kernel":
+            continue
+        assert re.search(r"\bpdl_wait(_then_release)?\s*\(\s*\)", body), f"{fn}: {name} never waits"
+
+
+def test_kernels_launch_through_the_launch_helpers():
+    """No triple-chevron launch but the plainly launched probe: every other
+    launch goes through launch_kernel / launch_kernel_as or the GEMM's own
+    cudaLaunchKernelEx, which set the overlap attribute."""
+    d = os.path.join(ROOT, "fp8_mixed_precision_gb300", "csrc")
+    sites = []
+    for fn in sorted(os.listdir(d)):
+        if fn.endswith((".cu", ".cuh", ".cpp", ".h")):
+            src = re.sub(r"//[^\n]*", " ", open(os.path.join(d, fn)).read())
+            sites += [(fn, m) for m in re.findall(r"(\w+)\s*<<<", src)]
+    assert sites == [("gemm.cu", "wait_timeout_probe_kernel")], sites
