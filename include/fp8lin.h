@@ -342,7 +342,7 @@ fp8_status fp8_grad_accumulate(float *acc, const void *dW, int64_t n, fp8_stream
  * fp8_linear_bwd, same recipe rules) whose inputs and results live in HOST
  * memory: the library copies them to and from the caller's device buffers.
  * Host buffers should be page-locked (cudaHostAlloc / pinned): pageable
- * memory works but then the copies stage through the driver and block.
+ * memory works but then the copies stage through the CUDA driver and block.
  *
  * A pipeline owns three CUDA streams on the device current at creation
  * (copy-in, compute, copy-out) and `slots` sets of events.  Each slot stands
