@@ -38,7 +38,8 @@ int num_sms();
 
 // Kernel launches allow programmatic dependent launch (the kernel may be
 // scheduled while the previous kernel on the stream drains; each kernel waits
-// for it in pdl_wait_then_release before touching global memory) unless the
+// for it in pdl_wait or pdl_wait_then_release before touching global memory,
+// see common.cuh) unless the
 // environment sets FP8LIN_PDL=0 when the library first launches.
 bool pdl_enabled();
 
